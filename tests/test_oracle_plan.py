@@ -1,0 +1,83 @@
+"""Pins for the oracle's tile plan (CPU)."""
+import numpy as np
+import pytest
+
+import oracle
+from long_context_masked_gb300 import inputs as I
+from tests._golden import load_plan_case
+
+
+def test_hand_worked_plan():
+    desc, tq, tk, exp = load_plan_case()
+    p = oracle.tile_plan_ref(desc, tq, tk)
+    for key, val in exp.items():
+        assert np.array_equal(p[key].astype(np.int64), val.astype(np.int64)), key
+
+
+def _tile_popcounts(m, tq, tk):
+    s = m.shape[0]
+    nq, nk = -(-s // tq), -(-s // tk)
+    out = np.zeros((nq, nk), np.int64)
+    area = np.zeros((nq, nk), np.int64)
+    for a in range(nq):
+        for b in range(nk):
+            blk = m[a * tq:(a + 1) * tq, b * tk:(b + 1) * tk]
+            out[a, b] = blk.sum()
+            area[a, b] = blk.size
+    return out, area
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_plan_consistent_with_mask(seed):
+    rng = np.random.default_rng(seed)
+    s = int(rng.integers(50, 400))
+    tq, tk = [(16, 16), (16, 32), (32, 16), (64, 64)][seed]
+    cu = I.cu_from_lengths(I.lognormal_doc_lengths(s, seed, mu=np.log(40), lo=5))
+    bm = I.uniform_block_map(s, 8, 3, 0.6, seed)
+    ro, co, vm = I.variable_block_map(s, 2, seed)
+    descs = [
+        I.MaskDesc(I.CAUSAL, s), I.MaskDesc(I.FULL, s),
+        I.MaskDesc(I.SLIDING_WINDOW, s, window=37),
+        I.MaskDesc(I.CAUSAL_DOCUMENT, s, cu_seqlens=cu),
+        I.MaskDesc(I.BLOCK_CAUSAL_DOCUMENT, s, block=12, cu_seqlens=cu),
+        I.MaskDesc(I.BLOCK_SPARSE_UNIFORM, s, block=8, map_heads=3, block_map=bm,
+                   n_row_blocks=bm.shape[1], n_col_blocks=bm.shape[2]),
+        I.MaskDesc(I.BLOCK_SPARSE_VARIABLE, s, base_causal=1, cu_seqlens=cu, map_heads=2,
+                   row_offsets=ro, col_offsets=co, block_map=vm,
+                   n_row_blocks=vm.shape[1], n_col_blocks=vm.shape[2]),
+    ]
+    for d in descs:
+        p = oracle.tile_plan_ref(d, tq, tk)
+        for hm in range(d.map_heads):
+            m = oracle.materialize_mask(d, hm)
+            pc, area = _tile_popcounts(m, tq, tk)
+            cls = p["cls"][hm]
+            assert ((cls == 0) == (pc == 0)).all()
+            assert ((cls == 1) == (pc == area)).all()
+            assert pc.sum() == oracle.n_valid_popcount(d, hm)
+        # CSR rows, CSR columns and the class array describe the same tiles
+        hmn, nq, nk = p["cls"].shape
+        rows = p["cls"].reshape(hmn * nq, nk)
+        for r in range(hmn * nq):
+            a, b = p["rowptr"][r], p["rowptr"][r + 1]
+            assert np.array_equal(p["kt_idx"][a:b], np.nonzero(rows[r])[0])
+            assert np.array_equal(p["kt_cls"][a:b], rows[r][rows[r] != 0])
+        cols = np.transpose(p["cls"], (0, 2, 1)).reshape(hmn * nk, nq)
+        for c in range(hmn * nk):
+            a, b = p["colptr"][c], p["colptr"][c + 1]
+            assert np.array_equal(p["qt_idx"][a:b], np.nonzero(cols[c])[0])
+        # longest first, ties by index, a permutation
+        for key, ptr in (("work_q", "rowptr"), ("work_k", "colptr")):
+            lens = np.diff(p[ptr])
+            w = p[key]
+            assert sorted(w.tolist()) == list(range(len(lens)))
+            pairs = list(zip(-lens[w], w))
+            assert pairs == sorted(pairs)
+
+
+def test_tile_rows_matches_full_plan():
+    s = 300
+    desc = I.MaskDesc(I.GLOBAL_SLIDING, s, num_global=20, window=50, base_causal=1)
+    p = oracle.tile_plan_ref(desc, 32, 64)
+    rows = oracle.tile_rows_ref(desc, 32, 64, 0, [0, 3, 9])
+    assert np.array_equal(rows, p["cls"][0, [0, 3, 9]])
