@@ -1,0 +1,342 @@
+// Forward pass of mask-aware exact softmax attention on sm_103a.
+//
+// Computes O = softmax(scale * Q K^T + mask) V and LSE per query row, the operation
+// the LongCA-bench kernels are measured on ("Long-Context Attention Benchmark":
+// summary page, abstract and sections 2.2 / 3.1; reading note, "Key design" 2).
+//
+// One CTA owns one 128-row query tile of one query head and walks that tile's list
+// of non-skipped key tiles (from the tile plan, longest lists launched first):
+//   warp 4      TMA producer: Q once, then K/V tiles into 2-stage rings;
+//   warp 5      TMEM owner and MMA issuer: S_n = Q K_n^T (tcgen05, fp32 in TMEM,
+//               double-buffered) and O += P_{n-1} V_{n-1} (accumulated in TMEM);
+//   warps 0-3   softmax, one query row per thread: read S_n from TMEM, apply the mask
+//               bits only on partial or ragged tiles, online softmax in fp32 with exp2,
+//               write P (bf16) into a 128-byte-swizzled shared tile for the PV MMA,
+//               rescale the O accumulator in TMEM when the running max moves by more
+//               than 2^8 (exact after the final 1/l normalisation), then the epilogue.
+// Tile = 128 x 128, head_dim = 128.  All waits are bounded.
+#include <cuda_runtime.h>
+
+#include "attn_kernels.h"
+#include "lca_device.cuh"
+
+namespace lca {
+
+namespace {
+
+constexpr int BM = 128;              // query rows per tile
+constexpr int BN = 128;              // keys per tile
+constexpr int HD = 128;              // head dim
+constexpr uint32_t TILE_BYTES = BM * HD * 2;   // 32 KB, two 128-byte-swizzled halves
+constexpr uint32_t HALF_BYTES = TILE_BYTES / 2;
+constexpr float RESCALE_THRESHOLD = 8.0f;      // log2 units
+
+// shared memory map (offsets from a 1024-aligned base)
+constexpr uint32_t OFF_Q = 0;
+constexpr uint32_t OFF_K = OFF_Q + TILE_BYTES;        // 2 stages
+constexpr uint32_t OFF_V = OFF_K + 2 * TILE_BYTES;    // 2 stages
+constexpr uint32_t OFF_P = OFF_V + 2 * TILE_BYTES;    // 2 buffers
+constexpr uint32_t OFF_BAR = OFF_P + 2 * TILE_BYTES;
+constexpr uint32_t SMEM_BYTES = OFF_BAR + 256 + 1024;  // + barriers + alignment slack
+
+// TMEM columns
+constexpr uint32_t TM_S0 = 0, TM_O = 256, TM_COLS = 512;
+
+struct Bars {
+  uint64_t q_full;
+  uint64_t k_full[2], k_empty[2];
+  uint64_t v_full[2], v_empty[2];
+  uint64_t s_full[2], p_ready[2], pv_done[2];
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, int kk) {
+  return desc_kmajor(tile, kk, HALF_BYTES);
+}
+__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile, int kk) {
+  return desc_mnmajor(tile, kk, HALF_BYTES);
+}
+
+__global__ void __launch_bounds__(192, 1)
+attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_v, FwdArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  const uint32_t base_u32 = (raw_u32 + 1023u) & ~1023u;
+  uint8_t* base = smem_raw + (base_u32 - raw_u32);
+  Bars& bar = *reinterpret_cast<Bars*>(base + OFF_BAR);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---- work item
+  const AttnDims& dm = a.dims;
+  const PlanDev& pl = a.plan;
+  const int per_item = dm.heads_per_map * dm.batch;
+  const int item = blockIdx.x / per_item;
+  const int rem = blockIdx.x - item * per_item;
+  const int sub = rem % dm.heads_per_map;
+  const int b = rem / dm.heads_per_map;
+  const int row = __ldg(pl.work_q + item);
+  const int hm = row / pl.n_qt;
+  const int qt = row - hm * pl.n_qt;
+  const int h = hm * dm.heads_per_map + sub;
+  const int hk = h / dm.group;
+  const int beg = __ldg(pl.rowptr + row);
+  const int n_tiles = __ldg(pl.rowptr + row + 1) - beg;
+  const int S = dm.seqlen;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bar.q_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bar.k_full[s], 1);
+      mbar_init(&bar.k_empty[s], 1);
+      mbar_init(&bar.v_full[s], 1);
+      mbar_init(&bar.v_empty[s], 1);
+      mbar_init(&bar.s_full[s], 1);
+      mbar_init(&bar.p_ready[s], BM);
+      mbar_init(&bar.pv_done[s], 1);
+    }
+    bar.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(&bar.tmem_base, TM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bar.tmem_base;
+  WaitCtx wc{&bar.abort, a.err, a.timeout_ns};
+
+  if (warp == 4) {
+    // ------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      mbar_arrive_expect_tx(&bar.q_full, TILE_BYTES);
+      for (int c = 0; c < 2; ++c)
+        tma_load_4d(base + OFF_Q + c * HALF_BYTES, &tm_q, &bar.q_full, c * 64, h, qt * BM, b);
+      for (int n = 0; n < n_tiles; ++n) {
+        const int kt = __ldg(pl.kt_idx + beg + n);
+        const int st = n & 1;
+        const uint32_t ph = (n >> 1) & 1;
+        if (n >= 2) mbar_wait(&bar.k_empty[st], ph ^ 1u, wc);
+        mbar_arrive_expect_tx(&bar.k_full[st], TILE_BYTES);
+        for (int c = 0; c < 2; ++c)
+          tma_load_4d(base + OFF_K + st * TILE_BYTES + c * HALF_BYTES, &tm_k, &bar.k_full[st],
+                      c * 64, hk, kt * BN, b);
+        if (n >= 2) mbar_wait(&bar.v_empty[st], ph ^ 1u, wc);
+        mbar_arrive_expect_tx(&bar.v_full[st], TILE_BYTES);
+        for (int c = 0; c < 2; ++c)
+          tma_load_4d(base + OFF_V + st * TILE_BYTES + c * HALF_BYTES, &tm_v, &bar.v_full[st],
+                      c * 64, hk, kt * BN, b);
+      }
+      if (bar.abort) {  // let copies in flight land before the CTA exits
+        mbar_wait_final(&bar.q_full, 0, a.timeout_ns);
+        for (int n = max(0, n_tiles - 2); n < n_tiles; ++n) {
+          mbar_wait_final(&bar.k_full[n & 1], (n >> 1) & 1, a.timeout_ns);
+          mbar_wait_final(&bar.v_full[n & 1], (n >> 1) & 1, a.timeout_ns);
+        }
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t IDESC_QK = idesc_bf16(BM, BN, 0, 0);
+      constexpr uint32_t IDESC_PV = idesc_bf16(BM, HD, 0, 1);
+      const uint32_t sq = base_u32 + OFF_Q;
+      auto issue_pv = [&](int j) {
+        const int st = j & 1;
+        const uint32_t ph = (j >> 1) & 1;
+        mbar_wait(&bar.p_ready[st], ph, wc);
+        mbar_wait(&bar.v_full[st], ph, wc);
+        tc_fence_after();
+        const uint32_t sp = base_u32 + OFF_P + st * TILE_BYTES;
+        const uint32_t sv = base_u32 + OFF_V + st * TILE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          umma_bf16_ss(tmem + TM_O, kmajor_desc(sp, kk), mnmajor_desc(sv, kk), IDESC_PV,
+                       (j > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&bar.pv_done[st]);
+        umma_commit(&bar.v_empty[st]);
+      };
+      mbar_wait(&bar.q_full, 0, wc);
+      for (int n = 0; n < n_tiles; ++n) {
+        const int st = n & 1;
+        const uint32_t ph = (n >> 1) & 1;
+        if (n >= 2) mbar_wait(&bar.p_ready[st], ph ^ 1u, wc);
+        mbar_wait(&bar.k_full[st], ph, wc);
+        tc_fence_after();
+        const uint32_t sk = base_u32 + OFF_K + st * TILE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk)
+          umma_bf16_ss(tmem + TM_S0 + st * BN, kmajor_desc(sq, kk), kmajor_desc(sk, kk), IDESC_QK,
+                       kk > 0 ? 1u : 0u);
+        umma_commit(&bar.s_full[st]);
+        umma_commit(&bar.k_empty[st]);
+        if (n >= 1) issue_pv(n - 1);
+      }
+      if (n_tiles >= 1) issue_pv(n_tiles - 1);
+    }
+  } else {
+    // ------------------------------------------------ softmax warps 0-3
+    const int t = threadIdx.x;  // row within the tile = TMEM lane
+    const int i = qt * BM + t;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const RowSpan sp = row_span(a.mask, min(i, S - 1));
+    const float sl2 = dm.scale_log2;
+    float m_run = -INFINITY;
+    float l_run = 0.f;
+    uint8_t* sP = base + OFF_P;
+
+    for (int n = 0; n < n_tiles; ++n) {
+      const int st = n & 1;
+      const uint32_t ph = (n >> 1) & 1;
+      const int kt = __ldg(pl.kt_idx + beg + n);
+      const int cls = __ldg(pl.kt_cls + beg + n);
+      mbar_wait(&bar.s_full[st], ph, wc);
+      __syncwarp();
+      tc_fence_after();
+      float s[BN];
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(lane_addr + TM_S0 + st * BN + c * 32, r);
+#pragma unroll
+        for (int x = 0; x < 32; ++x) s[c * 32 + x] = __uint_as_float(r[x]);
+      }
+      const int c0 = kt * BN;
+      if (cls != LCA_TILE_FULL || c0 + BN > S) {
+        uint32_t bits[BN / 32];
+        if (i < S) {
+          row_tile_bits<BN / 32>(a.mask, hm, i, c0, sp, bits);
+        } else {
+#pragma unroll
+          for (int w = 0; w < BN / 32; ++w) bits[w] = 0u;
+        }
+#pragma unroll
+        for (int x = 0; x < BN; ++x)
+          if (!((bits[x >> 5] >> (x & 31)) & 1u)) s[x] = -INFINITY;
+      }
+      float mx = s[0];
+#pragma unroll
+      for (int x = 1; x < BN; ++x) mx = fmaxf(mx, s[x]);
+      const float mt = mx * sl2;
+      float alpha = 1.f;
+      bool rescale = false;
+      if (mt > m_run + RESCALE_THRESHOLD) {
+        rescale = (l_run > 0.f);
+        alpha = ex2_approx(m_run - mt);
+        l_run *= alpha;
+        m_run = mt;
+      }
+      if (__any_sync(0xFFFFFFFFu, rescale)) {
+        // O holds P_0..P_{n-1} V: wait for the last PV, scale the row, store back
+        const int pj = n - 1;
+        mbar_wait(&bar.pv_done[pj & 1], (pj >> 1) & 1, wc);
+        __syncwarp();
+        tc_fence_after();
+        const float f = rescale ? alpha : 1.f;
+#pragma unroll
+        for (int c = 0; c < HD / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(lane_addr + TM_O + c * 32, r);
+#pragma unroll
+          for (int x = 0; x < 32; ++x) r[x] = __float_as_uint(__uint_as_float(r[x]) * f);
+          tmem_st32(lane_addr + TM_O + c * 32, r);
+        }
+      }
+      const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+      float lsum = 0.f;
+#pragma unroll
+      for (int x = 0; x < BN; ++x) {
+        s[x] = ex2_approx(fmaf(s[x], sl2, -m_use));
+        lsum += s[x];
+      }
+      l_run += lsum;
+      // P buffer st is free once PV_{n-2} completed
+      if (n >= 2) mbar_wait(&bar.pv_done[st], ph ^ 1u, wc);
+      __syncwarp();
+      const uint32_t p_tile = smem_u32(sP + st * TILE_BYTES);
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int x = hh * 64 + u * 8;
+          st_shared_v4(p_tile + hh * HALF_BYTES + sw128_offset(t, u),
+                       pack_bf16x2(s[x + 0], s[x + 1]), pack_bf16x2(s[x + 2], s[x + 3]),
+                       pack_bf16x2(s[x + 4], s[x + 5]), pack_bf16x2(s[x + 6], s[x + 7]));
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&bar.p_ready[st]);
+    }
+
+    // ---- epilogue: O = acc / l (bf16), LSE = (m + log2 l) * ln 2
+    if (n_tiles > 0) {
+      const int pj = n_tiles - 1;
+      mbar_wait(&bar.pv_done[pj & 1], (pj >> 1) & 1, wc);
+      __syncwarp();
+      tc_fence_after();
+    }
+    const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
+    __nv_bfloat16* orow = a.o + (static_cast<int64_t>(b) * S + i) * a.o_row_stride +
+                          static_cast<int64_t>(h) * HD;
+#pragma unroll
+    for (int c = 0; c < HD / 32; ++c) {
+      uint32_t r[32];
+      if (n_tiles > 0) {
+        tmem_ld32(lane_addr + TM_O + c * 32, r);
+      } else {
+#pragma unroll
+        for (int x = 0; x < 32; ++x) r[x] = 0u;
+      }
+      if (i < S) {
+        uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const int x = v * 8;
+          uint4 w;
+          w.x = pack_bf16x2(__uint_as_float(r[x + 0]) * inv, __uint_as_float(r[x + 1]) * inv);
+          w.y = pack_bf16x2(__uint_as_float(r[x + 2]) * inv, __uint_as_float(r[x + 3]) * inv);
+          w.z = pack_bf16x2(__uint_as_float(r[x + 4]) * inv, __uint_as_float(r[x + 5]) * inv);
+          w.w = pack_bf16x2(__uint_as_float(r[x + 6]) * inv, __uint_as_float(r[x + 7]) * inv);
+          dst[v] = w;
+        }
+      }
+    }
+    if (i < S) {
+      const float lse = (l_run > 0.f) ? (m_run + __log2f(l_run)) * 0.69314718055994531f
+                                      : -INFINITY;
+      a.lse[(static_cast<int64_t>(b) * dm.h_q + h) * S + i] = lse;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TM_COLS);
+  }
+}
+
+}  // namespace
+
+size_t fwd_smem_bytes() { return SMEM_BYTES; }
+
+cudaError_t launch_attn_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const FwdArgs& args, int n_blocks, cudaStream_t st) {
+  if (n_blocks == 0) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  attn_fwd_kernel<<<n_blocks, 192, SMEM_BYTES, st>>>(tq, tk, tv, args);
+  return cudaGetLastError();
+}
+
+}  // namespace lca

@@ -1,0 +1,57 @@
+// Host-side launchers and argument blocks of the attention kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "lca_types.h"
+
+namespace lca {
+
+struct FwdArgs {
+  AttnDims dims;
+  PlanDev plan;
+  MaskDev mask;
+  __nv_bfloat16* o;
+  float* lse;
+  int64_t o_row_stride;
+  unsigned int* err;
+  uint64_t timeout_ns;
+};
+
+struct BwdArgs {
+  AttnDims dims;
+  PlanDev plan;
+  MaskDev mask;
+  const __nv_bfloat16* o;
+  const __nv_bfloat16* dout;
+  const float* lse;
+  float* dsum;              // D = rowsum(dO * O), [B, H_q, S]
+  __nv_bfloat16* dq;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  int64_t o_row_stride;     // O, dO, dQ
+  int64_t k_row_stride;     // dK, dV
+  unsigned int* err;
+  uint64_t timeout_ns;
+};
+
+size_t fwd_smem_bytes();
+cudaError_t launch_attn_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const FwdArgs& args, int n_blocks, cudaStream_t st);
+
+cudaError_t launch_bwd_preprocess(const BwdArgs& args, cudaStream_t st);
+cudaError_t launch_bwd_dkdv(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tdo, const BwdArgs& args, int n_blocks,
+                            cudaStream_t st);
+cudaError_t launch_bwd_dq(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                          const CUtensorMap& tdo, const BwdArgs& args, int n_blocks,
+                          cudaStream_t st);
+
+cudaError_t launch_selftest_wait(unsigned int* err, uint64_t timeout_ns, cudaStream_t st);
+cudaError_t launch_selftest_umma(int variant, const CUtensorMap& ta, const CUtensorMap& tb,
+                                 const __nv_bfloat16* a_rowmajor, float* c, unsigned int* err,
+                                 cudaStream_t st);
+
+}  // namespace lca

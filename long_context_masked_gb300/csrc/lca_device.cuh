@@ -1,0 +1,398 @@
+// Device-side building blocks shared by the library's kernels: inline PTX for
+// mbarriers, TMA tile loads and the 5th-generation tensor cores (tcgen05 MMA with
+// TMEM accumulators), bounded waits, and the closed-form mask evaluation used by
+// the mask builder and by the attention kernels on partial tiles.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "lca_types.h"
+
+namespace lca {
+
+// ------------------------------------------------------------------ misc
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t elect_lane0() { return (threadIdx.x & 31) == 0; }
+
+// ------------------------------------------------------------------ mbarrier
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
+                   smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait state of one CTA: every wait is bounded by `timeout_ns`; the first wait that
+// runs out raises the CTA's abort flag (shared memory) and the device error word, and
+// every later wait of the CTA returns at once, so all threads drain to the end of the
+// kernel instead of hanging.
+struct WaitCtx {
+  volatile int* abort;    // shared memory, 0 = running
+  unsigned int* err;      // device error word
+  uint64_t timeout_ns;
+};
+
+static __device__ __noinline__ void mbar_wait_slow(uint64_t* bar, uint32_t parity, const WaitCtx& w) {
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t spins = 0;
+  while (!mbar_test(bar, parity)) {
+    if (*w.abort) return;
+    if ((++spins & 15u) == 0 && globaltimer_ns() - t0 > w.timeout_ns) {
+      *w.abort = 1;
+      atomicOr(w.err, LCA_DEVERR_TIMEOUT);
+      return;
+    }
+  }
+}
+
+__device__ __forceinline__ void mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtx& w) {
+  if (!mbar_test(bar, parity)) mbar_wait_slow(bar, parity, w);
+}
+
+// A last bounded wait that ignores the abort flag (used to let copies in flight land
+// before the CTA exits).
+static __device__ __noinline__ void mbar_wait_final(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_test(bar, parity)) {
+    if (globaltimer_ns() - t0 > timeout_ns) return;
+  }
+}
+
+// ------------------------------------------------------------------ fences
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// ------------------------------------------------------------------ TMA
+
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// 4-D tiled load (coordinates innermost first) completing on `bar` with byte count.
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int c0, int c1, int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2),
+      "r"(c3)
+      : "memory");
+}
+
+// ------------------------------------------------------------------ tcgen05
+
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+// Shared-memory matrix descriptor for a 128-byte-swizzled operand tile.
+// Bits: [0,14) start address >> 4, [16,30) leading byte offset >> 4, [32,46) stride byte
+// offset >> 4, [46,49) fixed 0b001, [61,64) swizzle mode (2 = 128-byte swizzle).
+// Tiles are 1024-byte aligned so the base-offset field stays 0.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
+// Descriptors of a 128-element-wide bf16 operand tile stored as two halves of 64
+// elements (128 bytes) per row, each half 128-byte swizzled, `half_bytes` apart
+// (rows * 128).  K-major: rows are M/N, the 128 elements are K; k-step kk (16
+// elements) starts kk%4 * 32 bytes into half kk/4 (leading offset unused).
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile, int kk, uint32_t half_bytes) {
+  return sdesc_sw128(tile + (kk >> 2) * half_bytes + (kk & 3) * 32, 16, 1024);
+}
+// MN-major: rows are K, the 128 elements are M/N; the two halves are the leading-offset
+// step along M/N and 8-row groups (1024 bytes) the stride-offset step along K; k-step kk
+// starts 16 rows = 2048 bytes further.
+__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int kk, uint32_t half_bytes) {
+  return sdesc_sw128(tile + kk * 2048, half_bytes, 1024);
+}
+
+// Instruction descriptor of kind::f16 with bf16 A/B and fp32 accumulation.
+// Bits: [4,6) D format (1 = f32), [7,10) A format (1 = bf16), [10,13) B format,
+// 15/16 A/B major (0 = K-major, 1 = MN-major), [17,23) N >> 3, [24,29) M >> 4.
+__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n, int a_mn, int b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn) << 15) |
+         (static_cast<uint32_t>(b_mn) << 16) | (static_cast<uint32_t>(n >> 3) << 17) |
+         (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.
+__device__ __forceinline__ void umma_bf16_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive once on `bar` when every tcgen05 op issued so far by this thread completes.
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+#define LCA_R8(b) "=r"(r[b + 0]), "=r"(r[b + 1]), "=r"(r[b + 2]), "=r"(r[b + 3]), \
+                  "=r"(r[b + 4]), "=r"(r[b + 5]), "=r"(r[b + 6]), "=r"(r[b + 7])
+#define LCA_W8(b) "r"(r[b + 0]), "r"(r[b + 1]), "r"(r[b + 2]), "r"(r[b + 3]), \
+                  "r"(r[b + 4]), "r"(r[b + 5]), "r"(r[b + 6]), "r"(r[b + 7])
+
+// 32 consecutive 32-bit TMEM columns of this thread's lane (lane = warp's quarter
+// base + lane id), waiting for completion inside the same asm statement.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, "
+      "[%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : LCA_R8(0), LCA_R8(8), LCA_R8(16), LCA_R8(24)
+      : "r"(taddr)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      LCA_W8(0), LCA_W8(8), LCA_W8(16), LCA_W8(24)
+      : "memory");
+}
+
+#undef LCA_R8
+#undef LCA_W8
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+
+// Byte offset of the 16-byte unit `u` (0..7) of row `r` inside a [rows][64] bf16 tile
+// stored with the 128-byte swizzle (the layout TMA writes for a 128-byte-wide box).
+__device__ __forceinline__ uint32_t sw128_offset(uint32_t r, uint32_t u) {
+  return r * 128u + ((u ^ (r & 7u)) << 4);
+}
+
+// ------------------------------------------------------------------ masks
+
+// Index s of the segment [cu[s], cu[s+1]) holding x, for 0 <= x < cu[n].
+__device__ __forceinline__ int seg_find(const int32_t* cu, int n, int x) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(cu + mid) <= x) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Allowed keys of query row i as two disjoint half-open intervals inside [0, S):
+// [a0, b0) and [a1, b1) (either may be empty).  Block-sparse masks return their base
+// interval (documents / causal), which the block map further restricts.
+struct RowSpan { int a0, b0, a1, b1; };
+
+__device__ __forceinline__ RowSpan row_span(const MaskDev& m, int i) {
+  RowSpan r{0, 0, 0, 0};
+  const int S = m.seqlen;
+  switch (m.type) {
+    case LCA_FULL: r.b0 = S; break;
+    case LCA_CAUSAL: r.b0 = i + 1; break;
+    case LCA_SLIDING_WINDOW: r.a0 = max(0, i - m.window + 1); r.b0 = i + 1; break;
+    case LCA_FULL_DOCUMENT: {
+      const int d = seg_find(m.cu, m.num_segments, i);
+      r.a0 = __ldg(m.cu + d); r.b0 = __ldg(m.cu + d + 1);
+    } break;
+    case LCA_CAUSAL_DOCUMENT: {
+      const int d = seg_find(m.cu, m.num_segments, i);
+      r.a0 = __ldg(m.cu + d); r.b0 = i + 1;
+    } break;
+    case LCA_PREFIX_LM: r.b0 = min(S, max(m.prefix_len, i + 1)); break;
+    case LCA_SHARED_QUESTION: {
+      const int s = seg_find(m.cu, m.num_segments, i);
+      if (s == 0) {
+        r.b0 = i + 1;
+      } else {
+        r.b0 = __ldg(m.cu + 1);
+        r.a1 = __ldg(m.cu + s); r.b1 = i + 1;
+      }
+    } break;
+    case LCA_GLOBAL_SLIDING: {
+      if (m.base_causal) {
+        const int g = min(m.num_global, i + 1);
+        const int wlo = max(0, i - m.window + 1);
+        if (wlo <= g) { r.b0 = i + 1; }
+        else { r.b0 = g; r.a1 = wlo; r.b1 = i + 1; }
+      } else if (i < m.num_global) {
+        r.b0 = S;
+      } else {
+        const int g = min(m.num_global, S);
+        const int wlo = max(0, i - m.window + 1);
+        const int whi = static_cast<int>(min(static_cast<long long>(S),
+                                             static_cast<long long>(i) + m.window));
+        if (wlo <= g) { r.b0 = whi; }
+        else { r.b0 = g; r.a1 = wlo; r.b1 = whi; }
+      }
+    } break;
+    case LCA_CAUSAL_BLOCKWISE:
+      r.b0 = static_cast<int>(min(static_cast<long long>(S),
+                                  (static_cast<long long>(i / m.block) + 1) * m.block));
+      break;
+    case LCA_BLOCK_CAUSAL_DOCUMENT: {
+      const int d = seg_find(m.cu, m.num_segments, i);
+      const int st = __ldg(m.cu + d), en = __ldg(m.cu + d + 1);
+      r.a0 = st;
+      r.b0 = static_cast<int>(min(static_cast<long long>(en),
+                                  st + (static_cast<long long>((i - st) / m.block) + 1) * m.block));
+    } break;
+    default: {  // block-sparse base
+      int lo = 0, hi = S;
+      if (m.num_segments > 0) {
+        const int d = seg_find(m.cu, m.num_segments, i);
+        lo = __ldg(m.cu + d); hi = __ldg(m.cu + d + 1);
+      }
+      if (m.base_causal) hi = min(hi, i + 1);
+      r.a0 = lo; r.b0 = hi;
+    } break;
+  }
+  if (r.b0 < r.a0) r.b0 = r.a0;
+  if (r.b1 < r.a1) r.b1 = r.a1;
+  return r;
+}
+
+__device__ __forceinline__ bool is_sparse(int type) {
+  return type == LCA_BLOCK_SPARSE_UNIFORM || type == LCA_BLOCK_SPARSE_VARIABLE;
+}
+
+// Bits of the columns [lo, hi) that fall into the 32 columns starting at ws.
+__device__ __forceinline__ uint32_t range_bits(int lo, int hi, int ws) {
+  const int a = max(lo - ws, 0);
+  const int b = min(hi - ws, 32);
+  if (b <= a) return 0u;
+  const uint32_t upper = (b >= 32) ? 0xFFFFFFFFu : ((1u << b) - 1u);
+  const uint32_t lower = (1u << a) - 1u;
+  return upper & ~lower;
+}
+
+// Allowed-key bits of row i over the NW*32 columns starting at c0 (bit c of word w =
+// column c0 + 32w + c).  Columns >= S are never allowed.
+template <int NW>
+__device__ __forceinline__ void row_tile_bits(const MaskDev& m, int h_m, int i, int c0,
+                                              const RowSpan& sp, uint32_t (&bits)[NW]) {
+#pragma unroll
+  for (int w = 0; w < NW; ++w)
+    bits[w] = range_bits(sp.a0, sp.b0, c0 + 32 * w) | range_bits(sp.a1, sp.b1, c0 + 32 * w);
+  if (!is_sparse(m.type)) return;
+  uint32_t mb[NW];
+#pragma unroll
+  for (int w = 0; w < NW; ++w) mb[w] = 0u;
+  const int c1 = min(c0 + NW * 32, m.seqlen);
+  if (m.type == LCA_BLOCK_SPARSE_UNIFORM) {
+    const int rb = i / m.block;
+    const uint8_t* row = m.bmap + (static_cast<size_t>(h_m) * m.n_rb + rb) * m.n_cb;
+    for (int cb = c0 / m.block; cb * m.block < c1; ++cb) {
+      if (__ldg(row + cb)) {
+        const int lo = cb * m.block, hi = lo + m.block;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) mb[w] |= range_bits(lo, hi, c0 + 32 * w);
+      }
+    }
+  } else {
+    const int32_t* ro = m.row_off + static_cast<size_t>(h_m) * (m.n_rb + 1);
+    const int32_t* co = m.col_off + static_cast<size_t>(h_m) * (m.n_cb + 1);
+    const int rb = seg_find(ro, m.n_rb, i);
+    const uint8_t* row = m.bmap + (static_cast<size_t>(h_m) * m.n_rb + rb) * m.n_cb;
+    for (int cb = seg_find(co, m.n_cb, c0); cb < m.n_cb; ++cb) {
+      const int lo = __ldg(co + cb);
+      if (lo >= c1) break;
+      if (__ldg(row + cb)) {
+        const int hi = __ldg(co + cb + 1);
+#pragma unroll
+        for (int w = 0; w < NW; ++w) mb[w] |= range_bits(lo, hi, c0 + 32 * w);
+      }
+    }
+  }
+#pragma unroll
+  for (int w = 0; w < NW; ++w) bits[w] &= mb[w];
+}
+
+}  // namespace lca

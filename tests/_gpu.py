@@ -1,0 +1,95 @@
+"""Shared helpers of the GPU parity tests (inputs, tolerance checks)."""
+import numpy as np
+import torch
+
+from long_context_masked_gb300 import inputs as I
+
+# Tolerances of the parity bar (bf16 inputs, fp32 accumulation):
+O_MAX_ABS = 1e-2         # forward output, max-abs
+LSE_MAX_ABS = 1e-3       # logsumexp (natural log), max-abs over finite rows
+GRAD_REL_FRO = 1e-2      # dQ / dK / dV, relative Frobenius error per tensor
+
+
+def bf16_half_ulp(x):
+    """Half a bf16 ulp of |x| (the rounding error bound of one bf16 output)."""
+    ax = np.maximum(np.abs(x), 1e-30)
+    e = np.floor(np.log2(ax))
+    return 0.5 * np.exp2(e - 7)
+
+
+def check_o(o_gpu, o_ref, what=""):
+    """Strict max-abs 1e-2; violations are tolerated only where |O_ref| >= 2, where
+    one bf16 rounding of the output alone exceeds 1e-2 (then error - half ulp <= 1e-2)."""
+    o_gpu = np.asarray(o_gpu, np.float64)
+    err = np.abs(o_gpu - o_ref)
+    bad = err > O_MAX_ABS
+    if bad.any():
+        assert (np.abs(o_ref[bad]) >= 2).all(), f"{what}: O max-abs {err.max():.3e}"
+        excess = (err - bf16_half_ulp(o_ref))[bad].max()
+        assert excess <= O_MAX_ABS, f"{what}: O excess over half ulp {excess:.3e}"
+    return float(err.max())
+
+
+def check_lse(l_gpu, l_ref, what=""):
+    l_gpu = np.asarray(l_gpu, np.float64)
+    inf_ref = ~np.isfinite(l_ref)
+    assert np.array_equal(~np.isfinite(l_gpu), inf_ref), f"{what}: empty-row pattern differs"
+    if inf_ref.any():
+        assert (l_gpu[inf_ref] < 0).all()
+    fin = ~inf_ref
+    err = np.abs(l_gpu[fin] - l_ref[fin]).max() if fin.any() else 0.0
+    assert err <= LSE_MAX_ABS, f"{what}: LSE max-abs {err:.3e}"
+    return float(err)
+
+
+def rel_fro(a, b):
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    den = np.linalg.norm(b)
+    return float(np.linalg.norm(a - b) / (den if den > 0 else 1.0))
+
+
+def check_grad(g_gpu, g_ref, what=""):
+    e = rel_fro(g_gpu, g_ref)
+    assert e <= GRAD_REL_FRO, f"{what}: relative Frobenius {e:.3e}"
+    return e
+
+
+def to_np(t):
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def make_inputs(b, s, hq, hkv, seed, device="cuda"):
+    q, k, v, do = I.qkv_do(b, s, hq, hkv, 128, seed)
+    host = [to_np(x) for x in (q, k, v, do)]
+    dev = [x.to(device) for x in (q, k, v, do)]
+    return host, dev
+
+
+def small_descs(s, hq, hkv, seed=0):
+    """One descriptor of every mask type at sequence length s."""
+    lens = I.lognormal_doc_lengths(s, seed, mu=np.log(max(64, s // 5)), lo=16)
+    cu = I.cu_from_lengths(lens)
+    q_len = max(1, s // 8)
+    rest = s - q_len
+    answers = [rest // 3, rest // 3, rest - 2 * (rest // 3)]
+    out = [
+        I.make_desc(I.FULL, s),
+        I.make_desc(I.CAUSAL, s),
+        I.make_desc(I.SLIDING_WINDOW, s, window=max(1, s // 5)),
+        I.make_desc(I.FULL_DOCUMENT, s, cu_seqlens=cu),
+        I.make_desc(I.CAUSAL_DOCUMENT, s, cu_seqlens=cu),
+        I.make_desc(I.PREFIX_LM, s),
+        I.make_desc(I.SHARED_QUESTION, s, question=q_len, answers=answers),
+        I.make_desc(I.GLOBAL_SLIDING, s, num_global=max(1, s // 20), window=max(1, s // 6)),
+        I.make_desc(I.GLOBAL_SLIDING, s, num_global=max(1, s // 20), window=max(1, s // 6),
+                    base_causal=0),
+        I.make_desc(I.CAUSAL_BLOCKWISE, s, block=max(1, s // 6)),
+        I.make_desc(I.BLOCK_CAUSAL_DOCUMENT, s, block=100, cu_seqlens=cu),
+        I.make_desc(I.BLOCK_SPARSE_UNIFORM, s, sparse_block=64, sparsity=0.5, map_heads=hkv,
+                    map_seed=seed),
+        I.make_desc(I.BLOCK_SPARSE_UNIFORM, s, sparse_block=128, sparsity=0.8, map_heads=hq,
+                    map_seed=seed + 1),
+        I.make_desc(I.BLOCK_SPARSE_VARIABLE, s, map_heads=hkv, map_seed=seed, cu_seqlens=cu),
+    ]
+    return out

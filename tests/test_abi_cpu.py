@@ -1,0 +1,86 @@
+"""The C-ABI library loads, exports every declared entry point and validates
+arguments on the host before touching the GPU (runs without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from long_context_masked_gb300 import binding
+from long_context_masked_gb300 import build as lca_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(binding.library_path()):
+        lca_build.build()
+    return binding.load_library()
+
+
+def _declared():
+    with open(os.path.join(ROOT, "include", "lca.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(lca_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert "lca_mask_build" in names and "lca_attn_fwd" in names and "lca_attn_bwd" in names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert lib.lca_status_string(code)
+    assert lib.lca_status_string(99) == b"unknown status"
+
+
+def _desc(**kw):
+    c = binding.MaskDescC()
+    c.type, c.seqlen = 1, 1024
+    for k, v in kw.items():
+        setattr(c, k, v)
+    return c
+
+
+@pytest.mark.parametrize("kw,tiles,expected", [
+    ({}, (32, 128), 2),                                  # unsupported tile
+    ({}, (128, 96), 2),
+    ({"seqlen": 0}, (128, 128), 1),
+    ({"seqlen": (1 << 20) + 1}, (128, 128), 2),
+    ({"type": 12}, (128, 128), 1),
+    ({"type": -1}, (128, 128), 1),
+    ({"type": 2, "window": 0}, (128, 128), 1),          # sliding window needs w >= 1
+    ({"type": 7, "window": 4, "num_global": -1}, (128, 128), 1),
+    ({"type": 5, "prefix_len": 1025}, (128, 128), 1),
+    ({"type": 8, "block": 0}, (128, 128), 1),
+    ({"type": 3, "num_segments": 0}, (128, 128), 1),    # documents need cu_seqlens
+    ({"type": 6, "num_segments": 2}, (128, 128), 1),    # ... and a pointer
+    ({"type": 10, "block": 64, "map_heads": 1, "n_row_blocks": 16, "n_col_blocks": 16,
+      "block_map": 0}, (128, 128), 1),                   # map pointer missing
+    ({"type": 10, "block": 64, "map_heads": 1, "n_row_blocks": 15, "n_col_blocks": 16,
+      "block_map": 16}, (128, 128), 1),                  # map size does not match S / block
+    ({"type": 11, "map_heads": 1, "n_row_blocks": 4, "n_col_blocks": 4, "block_map": 16},
+     (128, 128), 1),                                     # variable map without offsets
+])
+def test_mask_build_rejects_bad_descriptors(lib, kw, tiles, expected):
+    out = ctypes.c_void_p(123)
+    st = lib.lca_mask_build(ctypes.byref(_desc(**kw)), tiles[0], tiles[1], None, ctypes.byref(out))
+    assert st == expected
+    assert out.value is None
+
+
+def test_null_arguments(lib):
+    assert lib.lca_mask_build(None, 128, 128, None, ctypes.byref(ctypes.c_void_p())) == 1
+    assert lib.lca_mask_build(ctypes.byref(_desc()), 128, 128, None, None) == 1
+    sh = binding.ShapeC(1, 1024, 4, 4, 128, 512, 512, 512, 512)
+    assert lib.lca_attn_fwd(None, ctypes.byref(sh), 16, 16, 16, 16, 16, 0.0, None) == 1
+    assert lib.lca_attn_bwd(None, ctypes.byref(sh), *([16] * 10), 1 << 20, 0.0, 0, None) == 1
+    assert lib.lca_attn_bwd_workspace(None, ctypes.byref(sh), 0) == 0
+    info = binding.PlanInfoC()
+    assert lib.lca_plan_get_info(None, ctypes.byref(info)) == 1
+    lib.lca_plan_destroy(None)
