@@ -395,6 +395,7 @@ AttnDims make_dims(const lca_plan* p, const lca_shape* s, float softmax_scale) {
   d.h_kv = s->h_kv;
   d.group = s->h_q / s->h_kv;
   d.heads_per_map = s->h_q / p->info.map_heads;
+  d.kv_per_map = p->info.map_heads <= s->h_kv ? s->h_kv / p->info.map_heads : 0;
   d.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(s->head_dim));
   d.scale_log2 = d.scale * 1.4426950408889634f;
   return d;

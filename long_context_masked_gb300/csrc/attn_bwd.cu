@@ -1,5 +1,22 @@
-// Backward pass of mask-aware exact softmax attention on sm_103a (placeholder until
-// the dK/dV and dQ kernels land).
+// Backward pass of mask-aware exact softmax attention on sm_103a.
+//
+// The benchmark singles the backward pass out as the bottleneck of attention training
+// ("Long-Context Attention Benchmark": summary page, TL;DR and section 3.2; reading note,
+// key findings).  Given the forward's LSE, with P = exp(scale * Q K^T - LSE) under the
+// mask and D = rowsum(dO * O):
+//   dV = P^T dO,  dP = dO V^T,  dS = P * (dP - D),  dK = scale dS^T Q,  dQ = scale dS K.
+// Three kernels, deterministic and free of floating-point atomics:
+//   preprocess  D for every (b, h, i) row (HBM-bound);
+//   dK/dV       one CTA per (KV head, key tile): loops over the query tiles that attend
+//               to the key tile (the plan's transposed lists) for every query head of
+//               the KV group, recomputing S and dP with tcgen05 and accumulating dV and
+//               dK in TMEM;
+//   dQ          one CTA per (query head, query tile): loops over the tile's key tiles,
+//               recomputing S, dP and dS and accumulating dQ in TMEM.
+// Warp roles as in the forward: warp 4 issues TMA loads, warp 5 owns TMEM and issues
+// the MMAs, warps 0-3 (one query row per thread) turn S and dP into P and dS (bf16,
+// 128-byte-swizzled shared tiles).  The same shared P/dS tile is read K-major (as dS
+// for dQ) or MN-major (as P^T / dS^T for dV / dK).  All waits are bounded.
 #include <cuda_runtime.h>
 
 #include "attn_kernels.h"
@@ -7,14 +24,615 @@
 
 namespace lca {
 
-cudaError_t launch_bwd_preprocess(const BwdArgs&, cudaStream_t) { return cudaErrorNotSupported; }
-cudaError_t launch_bwd_dkdv(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
-                            const CUtensorMap&, const BwdArgs&, int, cudaStream_t) {
-  return cudaErrorNotSupported;
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 128;
+constexpr int HD = 128;
+constexpr uint32_t TILE = BM * HD * 2;
+constexpr uint32_t HALF = TILE / 2;
+constexpr float LOG2E = 1.4426950408889634f;
+
+// ------------------------------------------------------------------ preprocess
+
+__global__ void __launch_bounds__(256) bwd_preprocess_kernel(BwdArgs a) {
+  const int S = a.dims.seqlen, hq = a.dims.h_q;
+  const int64_t rows = static_cast<int64_t>(a.dims.batch) * S * hq;
+  const int64_t r = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 4;
+  const int part = threadIdx.x & 15;
+  float acc = 0.f;
+  if (r < rows) {
+    const int h = static_cast<int>(r % hq);
+    const int64_t bi = r / hq;
+    const int64_t off = bi * a.o_row_stride + h * HD + part * 8;
+    const uint4 ov = *reinterpret_cast<const uint4*>(a.o + off);
+    const uint4 gv = *reinterpret_cast<const uint4*>(a.dout + off);
+    const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
+    const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gv);
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      const float2 of = __bfloat1622float2(o2[x]);
+      const float2 gf = __bfloat1622float2(g2[x]);
+      acc = fmaf(of.x, gf.x, acc);
+      acc = fmaf(of.y, gf.y, acc);
+    }
+  }
+#pragma unroll
+  for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
+  if (part == 0 && r < rows) {
+    const int h = static_cast<int>(r % hq);
+    const int64_t bi = r / hq;
+    const int64_t b = bi / S, i = bi % S;
+    a.dsum[(b * hq + h) * S + i] = acc;
+  }
 }
-cudaError_t launch_bwd_dq(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
-                          const CUtensorMap&, const BwdArgs&, int, cudaStream_t) {
-  return cudaErrorNotSupported;
+
+// ------------------------------------------------------------------ shared pieces
+
+// P = exp2(s * scale_log2 - lse_log2) on allowed entries, dS = P (dP - D); packed to
+// bf16 pairs (P only when WANT_P).  Reads 32 columns of S and dP per step from TMEM.
+template <bool WANT_P>
+__device__ __forceinline__ void p_ds_rows(uint32_t s_addr, uint32_t dp_addr, bool masked,
+                                          const uint32_t (&bits)[4], float sl2, float lse2,
+                                          float dsum, uint32_t (&pk)[64], uint32_t (&dk)[64]) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t sr[32], dr[32];
+    tmem_ld32(s_addr + c * 32, sr);
+    tmem_ld32(dp_addr + c * 32, dr);
+#pragma unroll
+    for (int x = 0; x < 32; x += 2) {
+      float p0 = ex2_approx(fmaf(__uint_as_float(sr[x]), sl2, -lse2));
+      float p1 = ex2_approx(fmaf(__uint_as_float(sr[x + 1]), sl2, -lse2));
+      if (masked) {
+        if (!((bits[c] >> x) & 1u)) p0 = 0.f;
+        if (!((bits[c] >> (x + 1)) & 1u)) p1 = 0.f;
+      }
+      const float d0 = p0 * (__uint_as_float(dr[x]) - dsum);
+      const float d1 = p1 * (__uint_as_float(dr[x + 1]) - dsum);
+      if (WANT_P) pk[c * 16 + x / 2] = pack_bf16x2(p0, p1);
+      dk[c * 16 + x / 2] = pack_bf16x2(d0, d1);
+    }
+  }
+}
+
+// Store a row of 128 packed bf16 values into a [128][128] tile (two swizzled halves).
+__device__ __forceinline__ void store_row_tile(uint32_t tile, int row, const uint32_t (&v)[64]) {
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int x = hh * 32 + u * 4;
+      st_shared_v4(tile + hh * HALF + sw128_offset(row, u), v[x], v[x + 1], v[x + 2], v[x + 3]);
+    }
+}
+
+// Read a 128-column fp32 accumulator row from TMEM, scale, store 128 bf16 to global.
+__device__ __forceinline__ void store_acc_row(uint32_t taddr, bool have, float scale,
+                                              __nv_bfloat16* dst, bool write) {
+#pragma unroll
+  for (int c = 0; c < HD / 32; ++c) {
+    uint32_t r[32];
+    if (have) {
+      tmem_ld32(taddr + c * 32, r);
+    } else {
+#pragma unroll
+      for (int x = 0; x < 32; ++x) r[x] = 0u;
+    }
+    if (write) {
+      uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        const int x = v * 8;
+        uint4 w;
+        w.x = pack_bf16x2(__uint_as_float(r[x + 0]) * scale, __uint_as_float(r[x + 1]) * scale);
+        w.y = pack_bf16x2(__uint_as_float(r[x + 2]) * scale, __uint_as_float(r[x + 3]) * scale);
+        w.z = pack_bf16x2(__uint_as_float(r[x + 4]) * scale, __uint_as_float(r[x + 5]) * scale);
+        w.w = pack_bf16x2(__uint_as_float(r[x + 6]) * scale, __uint_as_float(r[x + 7]) * scale);
+        d4[v] = w;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ uint8_t* aligned_smem(uint8_t* raw, uint32_t& base_u32) {
+  const uint32_t raw_u32 = smem_u32(raw);
+  base_u32 = (raw_u32 + 1023u) & ~1023u;
+  return raw + (base_u32 - raw_u32);
+}
+
+// ------------------------------------------------------------------ dK / dV
+
+constexpr uint32_t KV_OFF_K = 0;
+constexpr uint32_t KV_OFF_V = TILE;
+constexpr uint32_t KV_OFF_Q = 2 * TILE;        // 2 stages
+constexpr uint32_t KV_OFF_DO = 4 * TILE;       // 2 stages
+constexpr uint32_t KV_OFF_PDS = 6 * TILE;
+constexpr uint32_t KV_OFF_BAR = 7 * TILE;
+constexpr uint32_t KV_SMEM = KV_OFF_BAR + 256 + 1024;
+constexpr uint32_t KV_TM_S = 0, KV_TM_DP = 128, KV_TM_DV = 256, KV_TM_DK = 384;
+
+struct KvBars {
+  uint64_t kv_full;
+  uint64_t q_full[2], q_empty[2], do_full[2], do_empty[2];
+  uint64_t sdp_full, sdp_free, p_ready, dv_done, ds_ready, dk_done;
+  uint32_t tmem_base;
+  int abort;
+};
+
+// Walks the (query head, query tile) pairs feeding one key tile: every query head of
+// the KV group, each with the transposed list of its map head.
+struct ColWalk {
+  const PlanDev* pl;
+  int kt, hk, group, heads_per_map, n_kt;
+  int gi, pos, end;
+  __device__ void start_head() {
+    const int h = hk * group + gi;
+    const int col = (h / heads_per_map) * n_kt + kt;
+    pos = __ldg(pl->colptr + col);
+    end = __ldg(pl->colptr + col + 1);
+  }
+  __device__ void init(const PlanDev* p, int kt_, int hk_, const AttnDims& d) {
+    pl = p; kt = kt_; hk = hk_; group = d.group; heads_per_map = d.heads_per_map; n_kt = p->n_kt;
+    gi = 0;
+    start_head();
+  }
+  // Next pair; false when done.
+  __device__ bool next(int& h, int& qt, int& cls) {
+    while (pos >= end) {
+      if (++gi >= group) return false;
+      start_head();
+    }
+    h = hk * group + gi;
+    qt = __ldg(pl->qt_idx + pos);
+    cls = __ldg(pl->qt_cls + pos);
+    ++pos;
+    return true;
+  }
+};
+
+__global__ void __launch_bounds__(192, 1)
+bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                BwdArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint32_t base_u32;
+  uint8_t* base = aligned_smem(smem_raw, base_u32);
+  KvBars& bar = *reinterpret_cast<KvBars*>(base + KV_OFF_BAR);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const AttnDims& dm = a.dims;
+  const PlanDev& pl = a.plan;
+  const int S = dm.seqlen;
+
+  int b, hk, kt;
+  if (dm.kv_per_map > 0) {
+    const int per_item = dm.kv_per_map * dm.batch;
+    const int item = blockIdx.x / per_item;
+    const int rem = blockIdx.x - item * per_item;
+    const int col = __ldg(pl.work_k + item);
+    const int hm = col / pl.n_kt;
+    kt = col - hm * pl.n_kt;
+    hk = hm * dm.kv_per_map + rem % dm.kv_per_map;
+    b = rem / dm.kv_per_map;
+  } else {
+    kt = blockIdx.x % pl.n_kt;
+    const int rest = blockIdx.x / pl.n_kt;
+    hk = rest % dm.h_kv;
+    b = rest / dm.h_kv;
+  }
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bar.kv_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bar.q_full[s], 1);
+      mbar_init(&bar.q_empty[s], 1);
+      mbar_init(&bar.do_full[s], 1);
+      mbar_init(&bar.do_empty[s], 1);
+    }
+    mbar_init(&bar.sdp_full, 1);
+    mbar_init(&bar.sdp_free, BM);
+    mbar_init(&bar.p_ready, BM);
+    mbar_init(&bar.dv_done, 1);
+    mbar_init(&bar.ds_ready, BM);
+    mbar_init(&bar.dk_done, 1);
+    bar.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(&bar.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bar.tmem_base;
+  WaitCtx wc{&bar.abort, a.err, a.timeout_ns};
+  ColWalk walk;
+  walk.init(&pl, kt, hk, dm);
+
+  if (warp == 4) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_do);
+      mbar_arrive_expect_tx(&bar.kv_full, 2 * TILE);
+      for (int c = 0; c < 2; ++c) {
+        tma_load_4d(base + KV_OFF_K + c * HALF, &tm_k, &bar.kv_full, c * 64, hk, kt * BN, b);
+        tma_load_4d(base + KV_OFF_V + c * HALF, &tm_v, &bar.kv_full, c * 64, hk, kt * BN, b);
+      }
+      int h, qt, cls, t = 0;
+      while (walk.next(h, qt, cls)) {
+        const int st = t & 1;
+        const uint32_t ph = (t >> 1) & 1;
+        if (t >= 2) mbar_wait(&bar.q_empty[st], ph ^ 1u, wc);
+        mbar_arrive_expect_tx(&bar.q_full[st], TILE);
+        for (int c = 0; c < 2; ++c)
+          tma_load_4d(base + KV_OFF_Q + st * TILE + c * HALF, &tm_q, &bar.q_full[st], c * 64, h,
+                      qt * BM, b);
+        if (t >= 2) mbar_wait(&bar.do_empty[st], ph ^ 1u, wc);
+        mbar_arrive_expect_tx(&bar.do_full[st], TILE);
+        for (int c = 0; c < 2; ++c)
+          tma_load_4d(base + KV_OFF_DO + st * TILE + c * HALF, &tm_do, &bar.do_full[st], c * 64, h,
+                      qt * BM, b);
+        ++t;
+      }
+      if (bar.abort) {
+        mbar_wait_final(&bar.kv_full, 0, a.timeout_ns);
+        for (int n = max(0, t - 2); n < t; ++n) {
+          mbar_wait_final(&bar.q_full[n & 1], (n >> 1) & 1, a.timeout_ns);
+          mbar_wait_final(&bar.do_full[n & 1], (n >> 1) & 1, a.timeout_ns);
+        }
+      }
+    }
+  } else if (warp == 5) {
+    if (lane == 0) {
+      constexpr uint32_t IDESC_NT = idesc_bf16(BM, BN, 0, 0);  // S, dP
+      constexpr uint32_t IDESC_TT = idesc_bf16(BN, HD, 1, 1);  // dV, dK (A, B MN-major)
+      const uint32_t sk = base_u32 + KV_OFF_K, sv = base_u32 + KV_OFF_V;
+      const uint32_t spds = base_u32 + KV_OFF_PDS;
+      int total = 0;
+      {
+        ColWalk w2 = walk;
+        int h, qt, cls;
+        while (w2.next(h, qt, cls)) ++total;
+      }
+      auto issue_sdp = [&](int t) {
+        const int st = t & 1;
+        const uint32_t ph = (t >> 1) & 1;
+        const uint32_t sq = base_u32 + KV_OFF_Q + st * TILE;
+        const uint32_t sdo = base_u32 + KV_OFF_DO + st * TILE;
+        mbar_wait(&bar.q_full[st], ph, wc);
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk)
+          umma_bf16_ss(tmem + KV_TM_S, desc_kmajor(sq, kk, HALF), desc_kmajor(sk, kk, HALF),
+                       IDESC_NT, kk > 0 ? 1u : 0u);
+        mbar_wait(&bar.do_full[st], ph, wc);
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk)
+          umma_bf16_ss(tmem + KV_TM_DP, desc_kmajor(sdo, kk, HALF), desc_kmajor(sv, kk, HALF),
+                       IDESC_NT, kk > 0 ? 1u : 0u);
+        umma_commit(&bar.sdp_full);
+      };
+      mbar_wait(&bar.kv_full, 0, wc);
+      if (total > 0) issue_sdp(0);
+      for (int t = 0; t < total; ++t) {
+        const int st = t & 1;
+        const uint32_t par = t & 1;
+        if (t + 1 < total) {
+          mbar_wait(&bar.sdp_free, par, wc);
+          issue_sdp(t + 1);
+        }
+        const uint32_t sq = base_u32 + KV_OFF_Q + st * TILE;
+        const uint32_t sdo = base_u32 + KV_OFF_DO + st * TILE;
+        mbar_wait(&bar.p_ready, par, wc);
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < BM / 16; ++kk)
+          umma_bf16_ss(tmem + KV_TM_DV, desc_mnmajor(spds, kk, HALF), desc_mnmajor(sdo, kk, HALF),
+                       IDESC_TT, (t > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&bar.dv_done);
+        umma_commit(&bar.do_empty[st]);
+        mbar_wait(&bar.ds_ready, par, wc);
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < BM / 16; ++kk)
+          umma_bf16_ss(tmem + KV_TM_DK, desc_mnmajor(spds, kk, HALF), desc_mnmajor(sq, kk, HALF),
+                       IDESC_TT, (t > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&bar.dk_done);
+        umma_commit(&bar.q_empty[st]);
+      }
+    }
+  } else {
+    const int tid = threadIdx.x;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const uint32_t spds = base_u32 + KV_OFF_PDS;
+    const float sl2 = dm.scale_log2;
+    const int c0 = kt * BN;
+    int h, qt, cls, t = 0;
+    while (walk.next(h, qt, cls)) {
+      const int i = qt * BM + tid;
+      const bool valid = i < S;
+      const int64_t rowi = (static_cast<int64_t>(b) * dm.h_q + h) * S + i;
+      float lse2 = INFINITY, dsum = 0.f;
+      if (valid) {
+        const float l = __ldg(a.lse + rowi);
+        lse2 = (l == -INFINITY) ? INFINITY : l * LOG2E;
+        dsum = __ldg(a.dsum + rowi);
+      }
+      const bool masked = cls != LCA_TILE_FULL || c0 + BN > S || qt * BM + BM > S;
+      uint32_t bits[4] = {0u, 0u, 0u, 0u};
+      if (masked && valid) {
+        const RowSpan sp = row_span(a.mask, i);
+        row_tile_bits<4>(a.mask, h / dm.heads_per_map, i, c0, sp, bits);
+      }
+      mbar_wait(&bar.sdp_full, t & 1, wc);
+      __syncwarp();
+      tc_fence_after();
+      uint32_t pk[64], dk[64];
+      p_ds_rows<true>(lane_addr + KV_TM_S, lane_addr + KV_TM_DP, masked, bits, sl2, lse2, dsum, pk, dk);
+      tc_fence_before();
+      mbar_arrive(&bar.sdp_free);
+      if (t >= 1) mbar_wait(&bar.dk_done, (t - 1) & 1, wc);
+      __syncwarp();
+      store_row_tile(spds, tid, pk);
+      fence_proxy_async_smem();
+      mbar_arrive(&bar.p_ready);
+      mbar_wait(&bar.dv_done, t & 1, wc);
+      __syncwarp();
+      store_row_tile(spds, tid, dk);
+      fence_proxy_async_smem();
+      mbar_arrive(&bar.ds_ready);
+      ++t;
+    }
+    if (t > 0) {
+      mbar_wait(&bar.dk_done, (t - 1) & 1, wc);
+      __syncwarp();
+      tc_fence_after();
+    }
+    const int j = kt * BN + tid;
+    const bool write = j < S;
+    const int64_t roff = (static_cast<int64_t>(b) * S + j) * a.k_row_stride +
+                         static_cast<int64_t>(hk) * HD;
+    store_acc_row(lane_addr + KV_TM_DV, t > 0, 1.f, a.dv + roff, write);
+    store_acc_row(lane_addr + KV_TM_DK, t > 0, dm.scale, a.dk + roff, write);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ------------------------------------------------------------------ dQ
+
+constexpr uint32_t DQ_OFF_Q = 0;
+constexpr uint32_t DQ_OFF_DO = TILE;
+constexpr uint32_t DQ_OFF_K = 2 * TILE;        // 2 stages
+constexpr uint32_t DQ_OFF_V = 4 * TILE;        // 2 stages
+constexpr uint32_t DQ_OFF_DS = 6 * TILE;
+constexpr uint32_t DQ_OFF_BAR = 7 * TILE;
+constexpr uint32_t DQ_SMEM = DQ_OFF_BAR + 256 + 1024;
+constexpr uint32_t DQ_TM_S = 0, DQ_TM_DP = 128, DQ_TM_DQ = 256;
+
+struct DqBars {
+  uint64_t qdo_full;
+  uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
+  uint64_t sdp_full, sdp_free, ds_ready, dq_done;
+  uint32_t tmem_base;
+  int abort;
+};
+
+__global__ void __launch_bounds__(192, 1)
+bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+              BwdArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint32_t base_u32;
+  uint8_t* base = aligned_smem(smem_raw, base_u32);
+  DqBars& bar = *reinterpret_cast<DqBars*>(base + DQ_OFF_BAR);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const AttnDims& dm = a.dims;
+  const PlanDev& pl = a.plan;
+  const int S = dm.seqlen;
+
+  const int per_item = dm.heads_per_map * dm.batch;
+  const int item = blockIdx.x / per_item;
+  const int rem = blockIdx.x - item * per_item;
+  const int row = __ldg(pl.work_q + item);
+  const int hm = row / pl.n_qt;
+  const int qt = row - hm * pl.n_qt;
+  const int h = hm * dm.heads_per_map + rem % dm.heads_per_map;
+  const int b = rem / dm.heads_per_map;
+  const int hk = h / dm.group;
+  const int beg = __ldg(pl.rowptr + row);
+  const int n_tiles = __ldg(pl.rowptr + row + 1) - beg;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bar.qdo_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bar.k_full[s], 1);
+      mbar_init(&bar.k_empty[s], 1);
+      mbar_init(&bar.v_full[s], 1);
+      mbar_init(&bar.v_empty[s], 1);
+    }
+    mbar_init(&bar.sdp_full, 1);
+    mbar_init(&bar.sdp_free, BM);
+    mbar_init(&bar.ds_ready, BM);
+    mbar_init(&bar.dq_done, 1);
+    bar.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(&bar.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bar.tmem_base;
+  WaitCtx wc{&bar.abort, a.err, a.timeout_ns};
+
+  if (warp == 4) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&bar.qdo_full, 2 * TILE);
+      for (int c = 0; c < 2; ++c) {
+        tma_load_4d(base + DQ_OFF_Q + c * HALF, &tm_q, &bar.qdo_full, c * 64, h, qt * BM, b);
+        tma_load_4d(base + DQ_OFF_DO + c * HALF, &tm_do, &bar.qdo_full, c * 64, h, qt * BM, b);
+      }
+      for (int n = 0; n < n_tiles; ++n) {
+        const int kt = __ldg(pl.kt_idx + beg + n);
+        const int st = n & 1;
+        const uint32_t ph = (n >> 1) & 1;
+        if (n >= 2) mbar_wait(&bar.k_empty[st], ph ^ 1u, wc);
+        mbar_arrive_expect_tx(&bar.k_full[st], TILE);
+        for (int c = 0; c < 2; ++c)
+          tma_load_4d(base + DQ_OFF_K + st * TILE + c * HALF, &tm_k, &bar.k_full[st], c * 64, hk,
+                      kt * BN, b);
+        if (n >= 2) mbar_wait(&bar.v_empty[st], ph ^ 1u, wc);
+        mbar_arrive_expect_tx(&bar.v_full[st], TILE);
+        for (int c = 0; c < 2; ++c)
+          tma_load_4d(base + DQ_OFF_V + st * TILE + c * HALF, &tm_v, &bar.v_full[st], c * 64, hk,
+                      kt * BN, b);
+      }
+      if (bar.abort) {
+        mbar_wait_final(&bar.qdo_full, 0, a.timeout_ns);
+        for (int n = max(0, n_tiles - 2); n < n_tiles; ++n) {
+          mbar_wait_final(&bar.k_full[n & 1], (n >> 1) & 1, a.timeout_ns);
+          mbar_wait_final(&bar.v_full[n & 1], (n >> 1) & 1, a.timeout_ns);
+        }
+      }
+    }
+  } else if (warp == 5) {
+    if (lane == 0) {
+      constexpr uint32_t IDESC_NT = idesc_bf16(BM, BN, 0, 0);  // S, dP
+      constexpr uint32_t IDESC_NN = idesc_bf16(BM, HD, 0, 1);  // dQ (B = K MN-major)
+      const uint32_t sq = base_u32 + DQ_OFF_Q, sdo = base_u32 + DQ_OFF_DO;
+      const uint32_t sds = base_u32 + DQ_OFF_DS;
+      auto issue_sdp = [&](int n) {
+        const int st = n & 1;
+        const uint32_t ph = (n >> 1) & 1;
+        const uint32_t sk = base_u32 + DQ_OFF_K + st * TILE;
+        const uint32_t sv = base_u32 + DQ_OFF_V + st * TILE;
+        mbar_wait(&bar.k_full[st], ph, wc);
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk)
+          umma_bf16_ss(tmem + DQ_TM_S, desc_kmajor(sq, kk, HALF), desc_kmajor(sk, kk, HALF),
+                       IDESC_NT, kk > 0 ? 1u : 0u);
+        mbar_wait(&bar.v_full[st], ph, wc);
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk)
+          umma_bf16_ss(tmem + DQ_TM_DP, desc_kmajor(sdo, kk, HALF), desc_kmajor(sv, kk, HALF),
+                       IDESC_NT, kk > 0 ? 1u : 0u);
+        umma_commit(&bar.sdp_full);
+        umma_commit(&bar.v_empty[st]);
+      };
+      mbar_wait(&bar.qdo_full, 0, wc);
+      if (n_tiles > 0) issue_sdp(0);
+      for (int n = 0; n < n_tiles; ++n) {
+        const int st = n & 1;
+        const uint32_t par = n & 1;
+        if (n + 1 < n_tiles) {
+          mbar_wait(&bar.sdp_free, par, wc);
+          issue_sdp(n + 1);
+        }
+        const uint32_t sk = base_u32 + DQ_OFF_K + st * TILE;
+        mbar_wait(&bar.ds_ready, par, wc);
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          umma_bf16_ss(tmem + DQ_TM_DQ, desc_kmajor(sds, kk, HALF), desc_mnmajor(sk, kk, HALF),
+                       IDESC_NN, (n > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&bar.dq_done);
+        umma_commit(&bar.k_empty[st]);
+      }
+    }
+  } else {
+    const int tid = threadIdx.x;
+    const int i = qt * BM + tid;
+    const bool valid = i < S;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const uint32_t sds = base_u32 + DQ_OFF_DS;
+    const float sl2 = dm.scale_log2;
+    const int64_t rowi = (static_cast<int64_t>(b) * dm.h_q + h) * S + i;
+    float lse2 = INFINITY, dsum = 0.f;
+    if (valid) {
+      const float l = __ldg(a.lse + rowi);
+      lse2 = (l == -INFINITY) ? INFINITY : l * LOG2E;
+      dsum = __ldg(a.dsum + rowi);
+    }
+    const RowSpan sp = row_span(a.mask, min(i, S - 1));
+    for (int n = 0; n < n_tiles; ++n) {
+      const int kt = __ldg(pl.kt_idx + beg + n);
+      const int cls = __ldg(pl.kt_cls + beg + n);
+      const int c0 = kt * BN;
+      const bool masked = cls != LCA_TILE_FULL || c0 + BN > S || qt * BM + BM > S;
+      uint32_t bits[4] = {0u, 0u, 0u, 0u};
+      if (masked && valid) row_tile_bits<4>(a.mask, hm, i, c0, sp, bits);
+      mbar_wait(&bar.sdp_full, n & 1, wc);
+      __syncwarp();
+      tc_fence_after();
+      uint32_t pk[64], dk[64];
+      p_ds_rows<false>(lane_addr + DQ_TM_S, lane_addr + DQ_TM_DP, masked, bits, sl2, lse2, dsum, pk, dk);
+      tc_fence_before();
+      mbar_arrive(&bar.sdp_free);
+      if (n >= 1) mbar_wait(&bar.dq_done, (n - 1) & 1, wc);
+      __syncwarp();
+      store_row_tile(sds, tid, dk);
+      fence_proxy_async_smem();
+      mbar_arrive(&bar.ds_ready);
+    }
+    if (n_tiles > 0) {
+      mbar_wait(&bar.dq_done, (n_tiles - 1) & 1, wc);
+      __syncwarp();
+      tc_fence_after();
+    }
+    const int64_t roff = (static_cast<int64_t>(b) * S + i) * a.o_row_stride +
+                         static_cast<int64_t>(h) * HD;
+    store_acc_row(lane_addr + DQ_TM_DQ, n_tiles > 0, dm.scale, a.dq + roff, valid);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_preprocess(const BwdArgs& a, cudaStream_t st) {
+  const int64_t rows = static_cast<int64_t>(a.dims.batch) * a.dims.seqlen * a.dims.h_q;
+  const int64_t blocks = (rows * 16 + 255) / 256;
+  bwd_preprocess_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dkdv(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tdo, const BwdArgs& a, int n_blocks,
+                            cudaStream_t st) {
+  if (n_blocks == 0) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, KV_SMEM);
+  if (e != cudaSuccess) return e;
+  bwd_dkdv_kernel<<<n_blocks, 192, KV_SMEM, st>>>(tq, tk, tv, tdo, a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dq(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                          const CUtensorMap& tdo, const BwdArgs& a, int n_blocks,
+                          cudaStream_t st) {
+  if (n_blocks == 0) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(bwd_dq_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, DQ_SMEM);
+  if (e != cudaSuccess) return e;
+  bwd_dq_kernel<<<n_blocks, 192, DQ_SMEM, st>>>(tq, tk, tv, tdo, a);
+  return cudaGetLastError();
 }
 
 }  // namespace lca

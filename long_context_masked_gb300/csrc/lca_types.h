@@ -39,6 +39,8 @@ struct PlanDev {
 struct AttnDims {
   int batch, seqlen, h_q, h_kv, group;  // group = h_q / h_kv
   int heads_per_map;                    // query heads sharing one map head
+  int kv_per_map;                       // KV heads per map head (0 when maps are per query head
+                                        // and a KV group spans several maps)
   float scale;                          // softmax scale
   float scale_log2;                     // scale * log2(e)
 };
