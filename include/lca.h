@@ -201,6 +201,21 @@ lca_status lca_selftest_wait_timeout(uint64_t timeout_ns, void* stream);
  * `stream`; returns the device status. */
 lca_status lca_selftest_umma(int variant, const void* a, const void* b, float* c, void* stream);
 
+/* Per-kernel timing (tracing).  While enabled, every kernel launch of the library is
+ * bracketed by two CUDA events recorded on the launch stream (no synchronisation is
+ * added).  lca_profile_read synchronises the device, writes up to `max_entries`
+ * records (one per kernel that launched since the last read: name, number of
+ * launches, summed event time in milliseconds) and clears the records; it returns the
+ * number of records written, or -1 on a CUDA error. */
+typedef struct {
+  char name[32];
+  int64_t launches;
+  double total_ms;
+} lca_kernel_time;
+
+void lca_profile_enable(int on);
+int lca_profile_read(lca_kernel_time* out, int max_entries);
+
 const char* lca_status_string(lca_status s);
 
 #ifdef __cplusplus

@@ -51,6 +51,11 @@ class PlanInfoC(ctypes.Structure):
                 ("n_partial", ctypes.c_int64)]
 
 
+class KernelTimeC(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 32), ("launches", ctypes.c_int64),
+                ("total_ms", ctypes.c_double)]
+
+
 _lib = None
 
 
@@ -83,6 +88,8 @@ def load_library():
         "lca_selftest_wait_timeout": ([u64, vp], i32),
         "lca_selftest_umma": ([ctypes.c_int, vp, vp, vp, vp], i32),
         "lca_status_string": ([i32], ctypes.c_char_p),
+        "lca_profile_enable": ([ctypes.c_int], None),
+        "lca_profile_read": ([ctypes.POINTER(KernelTimeC), ctypes.c_int], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -250,3 +257,17 @@ def selftest_umma(variant: int, a, b, stream=None):
 
 def selftest_wait_timeout(timeout_ns: int, stream=None) -> int:
     return load_library().lca_selftest_wait_timeout(timeout_ns, _stream(stream))
+
+
+def profile_enable(on: bool = True):
+    """Record CUDA events around every kernel launch of the library."""
+    load_library().lca_profile_enable(1 if on else 0)
+
+
+def profile_read() -> dict:
+    """{kernel name: (launches, total ms)} since the last read (synchronises)."""
+    buf = (KernelTimeC * 16)()
+    n = load_library().lca_profile_read(buf, 16)
+    if n < 0:
+        raise LcaError("lca_profile_read", 3)
+    return {buf[i].name.decode(): (int(buf[i].launches), float(buf[i].total_ms)) for i in range(n)}

@@ -14,6 +14,7 @@
 #include "attn_kernels.h"
 #include "lca_types.h"
 #include "mask_build.h"
+#include "profile.h"
 
 using namespace lca;
 
@@ -275,12 +276,24 @@ lca_status lca_mask_build(const lca_mask_desc* desc, int tile_q, int tile_k, voi
   if (!cuda_ok(cudaMemsetAsync(counters, 0, (hm_n + 1) * sizeof(unsigned long long), st)))
     return fail(LCA_ERR_CUDA);
 
-  if (!cuda_ok(launch_classify(m, tile_q, tile_k, n_qt, n_kt, cls, rowlen, counters,
-                               counters + hm_n, st)) ||
-      !cuda_ok(launch_scan(rowlen, n_rows, rowptr, st)) ||
-      !cuda_ok(launch_collen(cls, hm_n, n_qt, n_kt, collen, st)) ||
-      !cuda_ok(launch_scan(collen, n_cols, colptr, st)))
-    return fail(LCA_ERR_CUDA);
+  {
+    ProfScope ps(K_CLASSIFY, st);
+    if (!cuda_ok(launch_classify(m, tile_q, tile_k, n_qt, n_kt, cls, rowlen, counters,
+                                 counters + hm_n, st)))
+      return fail(LCA_ERR_CUDA);
+  }
+  {
+    ProfScope ps(K_SCAN, st);
+    if (!cuda_ok(launch_scan(rowlen, n_rows, rowptr, st))) return fail(LCA_ERR_CUDA);
+  }
+  {
+    ProfScope ps(K_COLLEN, st);
+    if (!cuda_ok(launch_collen(cls, hm_n, n_qt, n_kt, collen, st))) return fail(LCA_ERR_CUDA);
+  }
+  {
+    ProfScope ps(K_SCAN, st);
+    if (!cuda_ok(launch_scan(collen, n_cols, colptr, st))) return fail(LCA_ERR_CUDA);
+  }
 
   int32_t nnz = 0;
   unsigned long long n_partial = 0;
@@ -295,9 +308,17 @@ lca_status lca_mask_build(const lca_mask_desc* desc, int tile_q, int tile_k, voi
   int32_t* qt_idx = p->alloc<int32_t>(nnz);
   uint8_t* qt_cls = p->alloc<uint8_t>(nnz);
   if (!kt_idx || !kt_cls || !qt_idx || !qt_cls) return fail(LCA_ERR_OOM);
-  if (!cuda_ok(launch_fill(cls, hm_n, n_qt, n_kt, rowptr, kt_idx, kt_cls, colptr, qt_idx, qt_cls, st)) ||
-      !cuda_ok(launch_lpt(rowptr, n_rows, n_kt, work_q, colptr, n_cols, n_qt, work_k, st)))
-    return fail(LCA_ERR_CUDA);
+  {
+    ProfScope ps(K_FILL, st, 2);
+    if (!cuda_ok(launch_fill(cls, hm_n, n_qt, n_kt, rowptr, kt_idx, kt_cls, colptr, qt_idx,
+                             qt_cls, st)))
+      return fail(LCA_ERR_CUDA);
+  }
+  {
+    ProfScope ps(K_LPT, st);
+    if (!cuda_ok(launch_lpt(rowptr, n_rows, n_kt, work_q, colptr, n_cols, n_qt, work_k, st)))
+      return fail(LCA_ERR_CUDA);
+  }
 
   d.cls = cls;
   d.rowptr = rowptr;
@@ -429,9 +450,9 @@ lca_status lca_attn_fwd(const lca_plan* plan, const lca_shape* shape, const void
   a.timeout_ns = g_timeout_ns.load();
   if (!a.err) return LCA_ERR_CUDA;
   const int n_blocks = plan->info.n_qt * shape->h_q * shape->batch;
-  return launch_attn_fwd(tq, tk, tv, a, n_blocks, static_cast<cudaStream_t>(stream)) == cudaSuccess
-             ? LCA_OK
-             : LCA_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  ProfScope ps(K_FWD, st);
+  return launch_attn_fwd(tq, tk, tv, a, n_blocks, st) == cudaSuccess ? LCA_OK : LCA_ERR_CUDA;
 }
 
 size_t lca_attn_bwd_workspace(const lca_plan* plan, const lca_shape* shape, int flags) {
@@ -476,11 +497,20 @@ lca_status lca_attn_bwd(const lca_plan* plan, const lca_shape* shape, const void
   a.timeout_ns = g_timeout_ns.load();
   if (!a.err) return LCA_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (launch_bwd_preprocess(a, st) != cudaSuccess) return LCA_ERR_CUDA;
-  const int n_kv_blocks = plan->info.n_kt * shape->h_kv * shape->batch;
-  if (launch_bwd_dkdv(tq, tk, tv, tdo, a, n_kv_blocks, st) != cudaSuccess) return LCA_ERR_CUDA;
-  const int n_q_blocks = plan->info.n_qt * shape->h_q * shape->batch;
-  if (launch_bwd_dq(tq, tk, tv, tdo, a, n_q_blocks, st) != cudaSuccess) return LCA_ERR_CUDA;
+  {
+    ProfScope ps(K_BWD_PRE, st);
+    if (launch_bwd_preprocess(a, st) != cudaSuccess) return LCA_ERR_CUDA;
+  }
+  {
+    ProfScope ps(K_BWD_DKDV, st);
+    const int n_kv_blocks = plan->info.n_kt * shape->h_kv * shape->batch;
+    if (launch_bwd_dkdv(tq, tk, tv, tdo, a, n_kv_blocks, st) != cudaSuccess) return LCA_ERR_CUDA;
+  }
+  {
+    ProfScope ps(K_BWD_DQ, st);
+    const int n_q_blocks = plan->info.n_qt * shape->h_q * shape->batch;
+    if (launch_bwd_dq(tq, tk, tv, tdo, a, n_q_blocks, st) != cudaSuccess) return LCA_ERR_CUDA;
+  }
   return LCA_OK;
 }
 

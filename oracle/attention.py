@@ -98,12 +98,14 @@ def attn_fwd_ref(q, k, v, desc, *, scale: Optional[float] = None, chunk: int = 2
 
 
 def attn_bwd_ref(q, k, v, do, desc, *, scale: Optional[float] = None, chunk: int = 2048,
-                 heads: Optional[Sequence[int]] = None):
+                 heads: Optional[Sequence[int]] = None, row_range=None):
     """Forward plus analytic backward, fp64.
 
     Returns a dict with O, LSE, D, dQ, dK, dV in the library's layouts.  When
     ``heads`` is given only those query heads are processed (their dK/dV
-    contributions still land on their KV heads).
+    contributions still land on their KV heads); when ``row_range = (r0, r1)`` is
+    given only those query rows are processed, so dK/dV hold just their
+    contributions (used to time bounded samples).
     """
     b_n, s_len, h_q, d = q.shape
     h_kv = k.shape[2]
@@ -122,8 +124,9 @@ def attn_bwd_ref(q, k, v, do, desc, *, scale: Optional[float] = None, chunk: int
             hm = map_head_of(h, h_q, h_kv, desc.map_heads)
             kk = np.asarray(k[b, :, hk, :], np.float64)
             vv = np.asarray(v[b, :, hk, :], np.float64)
-            for r0 in range(0, s_len, chunk):
-                rows = np.arange(r0, min(s_len, r0 + chunk))
+            lo, hi = (0, s_len) if row_range is None else row_range
+            for r0 in range(lo, hi, chunk):
+                rows = np.arange(r0, min(hi, r0 + chunk))
                 qq = np.asarray(q[b, rows, h, :], np.float64)
                 gg = np.asarray(do[b, rows, h, :], np.float64)
                 m = mask_rows(desc, hm, rows)

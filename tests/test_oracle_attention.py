@@ -245,3 +245,16 @@ def test_row_functions_match_full():
         np.testing.assert_allclose(o2[a], r["O"][1, rows, h], atol=1e-13)
         np.testing.assert_allclose(lse2[a], r["LSE"][1, h, rows], atol=1e-13)
         np.testing.assert_allclose(dd[a], r["D"][1, h, rows], atol=1e-13)
+
+
+def test_row_range_restriction_is_a_slice_of_the_full_result():
+    rng = np.random.default_rng(17)
+    s, d = 40, 4
+    desc = I.MaskDesc(I.CAUSAL_DOCUMENT, s, cu_seqlens=np.array([0, 13, 40], np.int32))
+    q, k, v, do = (_rand((1, s, 2, d), rng) for _ in range(4))
+    full = oracle.attn_bwd_ref(q, k, v, do, desc, chunk=7)
+    parts = [oracle.attn_bwd_ref(q, k, v, do, desc, chunk=7, row_range=r) for r in ((0, 17), (17, 40))]
+    np.testing.assert_allclose(parts[0]["dQ"][:, :17] + parts[1]["dQ"][:, :17], full["dQ"][:, :17],
+                               atol=1e-13)
+    np.testing.assert_allclose(parts[0]["dK"] + parts[1]["dK"], full["dK"], atol=1e-13)
+    np.testing.assert_allclose(parts[0]["dV"] + parts[1]["dV"], full["dV"], atol=1e-13)
