@@ -181,6 +181,29 @@ lca_status lca_attn_bwd(const lca_plan* plan, const lca_shape* shape, const void
                         const float* lse, void* dq, void* dk, void* dv, void* workspace,
                         size_t ws_bytes, float softmax_scale, int flags, void* stream);
 
+/* Backward pass that allocates nothing, for callers that cannot allocate device memory
+ * when they run the backward (inside CUDA-graph capture, under allocators that forbid
+ * side allocations, or in runtimes that only hand out the op's own tensors).  The
+ * attention method itself has no counterpart of this call: it only changes where the
+ * workspace of lca_attn_bwd comes from.
+ *
+ * Same arguments, preconditions and results as lca_attn_bwd (flags 0), except that
+ * the D workspace is a fixed 32 MiB buffer compiled into the library (a file-scope
+ * device array that every GPU loading the library holds until the process exits),
+ * so it serves at most batch * h_q * seqlen <= 2^23 rows; larger shapes return
+ * LCA_ERR_UNSUPPORTED without launching anything.  No cudaMalloc / cudaFree is made
+ * (with lca_profile_enable on, the timing events of the launches come from a pool
+ * that grows on first use).
+ * The first call on a device looks the buffer's device address up (once per device,
+ * with that device current); make that first call before any stream capture.
+ * Every call on a device shares the one buffer: each call overwrites every entry it
+ * reads, so nothing needs clearing, but calls whose work overlaps on the GPU (other
+ * streams, other threads) race on it and must be serialised by the caller. */
+lca_status lca_attn_bwd_noalloc(const lca_plan* plan, const lca_shape* shape, const void* q,
+                                const void* k, const void* v, const void* o, const void* dout,
+                                const float* lse, void* dq, void* dk, void* dv,
+                                float softmax_scale, void* stream);
+
 /* Synchronise `stream`, read and clear the device error word: LCA_OK, or
  * LCA_ERR_TIMEOUT when a bounded device wait ran out since the last call. */
 lca_status lca_get_last_device_error(void* stream);

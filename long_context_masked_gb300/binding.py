@@ -88,6 +88,7 @@ def load_library():
         "lca_selftest_wait_timeout": ([u64, vp], i32),
         "lca_selftest_umma": ([ctypes.c_int, vp, vp, vp, vp], i32),
         "lca_status_string": ([i32], ctypes.c_char_p),
+        "lca_attn_bwd_noalloc": ([vp, ctypes.POINTER(ShapeC)] + [vp] * 9 + [f32, vp], i32),
         "lca_profile_enable": ([ctypes.c_int], None),
         "lca_profile_read": ([ctypes.POINTER(KernelTimeC), ctypes.c_int], ctypes.c_int),
     }
@@ -238,6 +239,29 @@ def attn_bwd(plan: Plan, q, k, v, o, do, lse, scale: Optional[float] = None, dq=
                           workspace.numel() * workspace.element_size(),
                           float(scale) if scale else 0.0, 0, _stream(stream))
     _check("lca_attn_bwd", st)
+    return dq, dk, dv
+
+
+def attn_bwd_noalloc(plan: Plan, q, k, v, o, do, lse, scale: Optional[float] = None, dq=None,
+                     dk=None, dv=None, stream=None):
+    """dQ, dK, dV through lca_attn_bwd_noalloc: the backward for callers that cannot
+    allocate device memory at that point; its workspace is the library's fixed
+    built-in buffer (batch * h_q * seqlen <= 2^23).  Pass preallocated dq/dk/dv to
+    keep the call free of allocations on the Python side too."""
+    import torch
+
+    lib = load_library()
+    if do.stride() != o.stride():
+        raise LcaError("dO must have the layout of O", 1)
+    sh = _shape(q, k, v, o)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    st = lib.lca_attn_bwd_noalloc(plan.handle, ctypes.byref(sh), q.data_ptr(), k.data_ptr(),
+                                  v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
+                                  dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                                  float(scale) if scale else 0.0, _stream(stream))
+    _check("lca_attn_bwd_noalloc", st)
     return dq, dk, dv
 
 

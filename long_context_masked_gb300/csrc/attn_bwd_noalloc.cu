@@ -1,0 +1,61 @@
+// lca_attn_bwd_noalloc: the backward pass for callers that cannot allocate device
+// memory.
+//
+// lca_attn_bwd needs a caller-provided workspace (the per-row D = rowsum(dO * O)
+// buffer, fp32 [batch, h_q, seqlen]).  Some callers cannot call cudaMalloc at that
+// point: code running while a CUDA graph is being captured on their stream, custom
+// allocators that forbid side allocations, or runtimes that hand out only the
+// tensors of the op itself.  This entry point takes the workspace from a fixed
+// buffer compiled into the library instead, and otherwise runs exactly the
+// lca_attn_bwd path.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "../../include/lca.h"
+
+namespace {
+
+// Capacity of the built-in workspace in rows of D (batch * h_q * seqlen), 32 MiB.
+constexpr size_t kMaxRows = size_t(1) << 23;
+
+// The buffer lives in every GPU that loads the library, for the life of the process.
+static __device__ __align__(256) float g_bwd_scratch[kMaxRows];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+float* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of g_bwd_scratch on the current device, looked up once per device.
+// In host code the symbol name is only a host-side handle, never a device address.
+lca_status scratch_on_current_device(float** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return LCA_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_bwd_scratch) != cudaSuccess || !p) return LCA_ERR_CUDA;
+    g_scratch_ptr[dev] = static_cast<float*>(p);
+  }
+  *out = g_scratch_ptr[dev];
+  return LCA_OK;
+}
+
+}  // namespace
+
+extern "C" lca_status lca_attn_bwd_noalloc(const lca_plan* plan, const lca_shape* shape,
+                                           const void* q, const void* k, const void* v,
+                                           const void* o, const void* dout, const float* lse,
+                                           void* dq, void* dk, void* dv, float softmax_scale,
+                                           void* stream) {
+  if (!plan || !shape) return LCA_ERR_INVALID_ARG;
+  if (shape->batch < 1 || shape->h_q < 1 || shape->seqlen < 1) return LCA_ERR_INVALID_ARG;
+  const size_t rows = static_cast<size_t>(shape->batch) * static_cast<size_t>(shape->h_q) *
+                      static_cast<size_t>(shape->seqlen);
+  if (rows > kMaxRows) return LCA_ERR_UNSUPPORTED;
+  float* scratch = nullptr;
+  lca_status s = scratch_on_current_device(&scratch);
+  if (s != LCA_OK) return s;
+  return lca_attn_bwd(plan, shape, q, k, v, o, dout, lse, dq, dk, dv, scratch,
+                      kMaxRows * sizeof(float), softmax_scale, 0, stream);
+}

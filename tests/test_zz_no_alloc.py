@@ -1,0 +1,48 @@
+"""lca_attn_bwd_noalloc, the backward for callers that cannot allocate device memory
+(CUDA-graph capture, restrictive allocators): through the C ABI it must give the
+results of lca_attn_bwd, on consecutive calls that share its built-in workspace.
+
+This file is collected last so that a failure here never hides another test."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import long_context_masked_gb300 as lca
+from long_context_masked_gb300 import binding
+from long_context_masked_gb300 import inputs as I
+from tests._gpu import GRAD_REL_FRO, make_inputs, rel_fro, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+def test_noalloc_backward_matches_allocating_backward_twice():
+    s, hq, hkv = 1408, 8, 2
+    _, dev = make_inputs(1, s, hq, hkv, seed=77)
+    q, k, v, do = dev
+    desc = I.make_desc(I.CAUSAL_DOCUMENT, s, doc_seed=3)
+    plan = lca.mask_build(desc, 128, 128)
+    o, lse = lca.attn_fwd(plan, q, k, v)
+    ref = lca.attn_bwd(plan, q, k, v, o, do, lse)
+    torch.cuda.synchronize()
+    outs = [(torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)) for _ in range(2)]
+    for dq, dk, dv in outs:      # two calls in a row on the shared built-in buffer
+        lca.attn_bwd_noalloc(plan, q, k, v, o, do, lse, dq=dq, dk=dk, dv=dv)
+    assert lca.last_device_error() == 0
+    for got in outs:
+        for g, r in zip(got, ref):
+            assert rel_fro(to_np(g), to_np(r)) <= GRAD_REL_FRO
+
+
+def test_noalloc_backward_rejects_shapes_beyond_its_buffer():
+    lib = binding.load_library()
+    s = 131073                      # 64 heads x 131073 rows > 2^23 rows of D
+    plan = lca.mask_build(I.make_desc(I.FULL, s), 128, 128)
+    sh = binding.ShapeC(1, s, 64, 8, 128, 64 * 128, 8 * 128, 8 * 128, 64 * 128)
+    dummy = torch.empty(16, dtype=torch.bfloat16, device="cuda")
+    p = dummy.data_ptr()
+    st = lib.lca_attn_bwd_noalloc(plan.handle, ctypes.byref(sh), p, p, p, p, p, p, p, p, p,
+                                  0.0, None)
+    assert st == 2                  # LCA_ERR_UNSUPPORTED, nothing launched
+    assert lca.last_device_error() == 0
