@@ -220,7 +220,8 @@ lca_status lca_selftest_wait_timeout(uint64_t timeout_ns, void* stream);
  * fp32 accumulation on one CTA.  a, b: device bf16 [128][128] row-major; c: device
  * fp32 [128][128] row-major output.  variant 0: c = a b^T (both loaded K-major by TMA);
  * 1: c = a b (b loaded MN-major); 2: c = a b with a written to shared memory by the
- * threads in the 128-byte swizzle; 3: c = a^T b (a loaded MN-major).  Synchronises
+ * threads in the 128-byte swizzle; 3: c = a^T b (a loaded MN-major); 4: c = a b with a
+ * held in tensor memory (written by the threads with tcgen05.st).  Synchronises
  * `stream`; returns the device status. */
 lca_status lca_selftest_umma(int variant, const void* a, const void* b, float* c, void* stream);
 

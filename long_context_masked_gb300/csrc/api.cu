@@ -534,7 +534,7 @@ lca_status lca_selftest_wait_timeout(uint64_t timeout_ns, void* stream) {
 }
 
 lca_status lca_selftest_umma(int variant, const void* a, const void* b, float* c, void* stream) {
-  if (variant < 0 || variant > 3 || !a || !b || !c) return LCA_ERR_INVALID_ARG;
+  if (variant < 0 || variant > 4 || !a || !b || !c) return LCA_ERR_INVALID_ARG;
   CUtensorMap ta, tb;
   if (!make_tmap_bshd(&ta, a, 1, 128, 1, 128, 128) || !make_tmap_bshd(&tb, b, 1, 128, 1, 128, 128))
     return LCA_ERR_CUDA;

@@ -13,8 +13,10 @@
 //               dK in TMEM;
 //   dQ          one CTA per (query head, query tile): loops over the tile's key tiles,
 //               recomputing S, dP and dS and accumulating dQ in TMEM.
-// Warp roles as in the forward: warp 4 issues TMA loads, warp 5 owns TMEM and issues
-// the MMAs, warps 0-3 (one query row per thread) turn S and dP into P and dS (bf16,
+// Warp roles as in the forward: warp 8 issues TMA loads, warp 9 owns TMEM and issues
+// the MMAs, warps 0-7 (two threads per query row, 64 key columns each) load their
+// halves of S and dP from TMEM behind one wait - which frees both accumulators at once,
+// so the next S/dP MMAs overlap the exp work - and turn them into P and dS (bf16,
 // 128-byte-swizzled shared tiles).  The same shared P/dS tile is read K-major (as dS
 // for dQ) or MN-major (as P^T / dS^T for dV / dK).  All waits are bounded.
 #include <cuda_runtime.h>
@@ -69,68 +71,63 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(BwdArgs a) {
 
 // ------------------------------------------------------------------ shared pieces
 
-// P = exp2(s * scale_log2 - lse_log2) on allowed entries, dS = P (dP - D); packed to
-// bf16 pairs (P only when WANT_P).  Reads 32 columns of S and dP per step from TMEM.
+constexpr int NUM_THREADS = 320;     // 8 softmax warps, producer, MMA issuer
+constexpr int SOFTMAX_THREADS = 256;
+constexpr int WARP_PRODUCER = 8, WARP_MMA = 9;
+
+// Half a row (64 key columns) of P = exp2(s * scale_log2 - lse_log2) on allowed
+// entries and dS = P (dP - D), packed to bf16 pairs (P only when WANT_P).
 template <bool WANT_P>
-__device__ __forceinline__ void p_ds_rows(uint32_t s_addr, uint32_t dp_addr, bool masked,
-                                          const uint32_t (&bits)[4], float sl2, float lse2,
-                                          float dsum, uint32_t (&pk)[64], uint32_t (&dk)[64]) {
+__device__ __forceinline__ void p_ds_half(const uint32_t (&sr)[64], const uint32_t (&dr)[64],
+                                          bool masked, const uint32_t (&bits)[2], float sl2,
+                                          float lse2, float dsum, uint32_t (&pk)[32],
+                                          uint32_t (&dk)[32]) {
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    uint32_t sr[32], dr[32];
-    tmem_ld32(s_addr + c * 32, sr);
-    tmem_ld32(dp_addr + c * 32, dr);
-#pragma unroll
-    for (int x = 0; x < 32; x += 2) {
-      float p0 = ex2_approx(fmaf(__uint_as_float(sr[x]), sl2, -lse2));
-      float p1 = ex2_approx(fmaf(__uint_as_float(sr[x + 1]), sl2, -lse2));
-      if (masked) {
-        if (!((bits[c] >> x) & 1u)) p0 = 0.f;
-        if (!((bits[c] >> (x + 1)) & 1u)) p1 = 0.f;
-      }
-      const float d0 = p0 * (__uint_as_float(dr[x]) - dsum);
-      const float d1 = p1 * (__uint_as_float(dr[x + 1]) - dsum);
-      if (WANT_P) pk[c * 16 + x / 2] = pack_bf16x2(p0, p1);
-      dk[c * 16 + x / 2] = pack_bf16x2(d0, d1);
+  for (int x = 0; x < 64; x += 2) {
+    float p0 = ex2_approx(fmaf(__uint_as_float(sr[x]), sl2, -lse2));
+    float p1 = ex2_approx(fmaf(__uint_as_float(sr[x + 1]), sl2, -lse2));
+    if (masked) {
+      if (!((bits[x >> 5] >> (x & 31)) & 1u)) p0 = 0.f;
+      if (!((bits[x >> 5] >> ((x + 1) & 31)) & 1u)) p1 = 0.f;
     }
+    const float d0 = p0 * (__uint_as_float(dr[x]) - dsum);
+    const float d1 = p1 * (__uint_as_float(dr[x + 1]) - dsum);
+    if (WANT_P) pk[x / 2] = pack_bf16x2(p0, p1);
+    dk[x / 2] = pack_bf16x2(d0, d1);
   }
 }
 
-// Store a row of 128 packed bf16 values into a [128][128] tile (two swizzled halves).
-__device__ __forceinline__ void store_row_tile(uint32_t tile, int row, const uint32_t (&v)[64]) {
+// Store half a row (64 packed bf16 pairs -> 64 columns) into one swizzled [128][64]
+// half of a [128][128] tile.
+__device__ __forceinline__ void store_half_row(uint32_t half_tile, int row,
+                                               const uint32_t (&v)[32]) {
 #pragma unroll
-  for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int x = hh * 32 + u * 4;
-      st_shared_v4(tile + hh * HALF + sw128_offset(row, u), v[x], v[x + 1], v[x + 2], v[x + 3]);
-    }
+  for (int u = 0; u < 8; ++u)
+    st_shared_v4(half_tile + sw128_offset(row, u), v[u * 4], v[u * 4 + 1], v[u * 4 + 2],
+                 v[u * 4 + 3]);
 }
 
-// Read a 128-column fp32 accumulator row from TMEM, scale, store 128 bf16 to global.
-__device__ __forceinline__ void store_acc_row(uint32_t taddr, bool have, float scale,
-                                              __nv_bfloat16* dst, bool write) {
+// Read 64 fp32 accumulator columns of this thread's lane, scale, store 64 bf16.
+__device__ __forceinline__ void store_acc_half(uint32_t taddr, bool have, float scale,
+                                               __nv_bfloat16* dst, bool write) {
+  uint32_t r[64];
+  if (have) {
+    tmem_ld64(taddr, r);
+  } else {
 #pragma unroll
-  for (int c = 0; c < HD / 32; ++c) {
-    uint32_t r[32];
-    if (have) {
-      tmem_ld32(taddr + c * 32, r);
-    } else {
+    for (int x = 0; x < 64; ++x) r[x] = 0u;
+  }
+  if (write) {
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
-      for (int x = 0; x < 32; ++x) r[x] = 0u;
-    }
-    if (write) {
-      uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
-#pragma unroll
-      for (int v = 0; v < 4; ++v) {
-        const int x = v * 8;
-        uint4 w;
-        w.x = pack_bf16x2(__uint_as_float(r[x + 0]) * scale, __uint_as_float(r[x + 1]) * scale);
-        w.y = pack_bf16x2(__uint_as_float(r[x + 2]) * scale, __uint_as_float(r[x + 3]) * scale);
-        w.z = pack_bf16x2(__uint_as_float(r[x + 4]) * scale, __uint_as_float(r[x + 5]) * scale);
-        w.w = pack_bf16x2(__uint_as_float(r[x + 6]) * scale, __uint_as_float(r[x + 7]) * scale);
-        d4[v] = w;
-      }
+    for (int v = 0; v < 8; ++v) {
+      const int x = v * 8;
+      uint4 w;
+      w.x = pack_bf16x2(__uint_as_float(r[x + 0]) * scale, __uint_as_float(r[x + 1]) * scale);
+      w.y = pack_bf16x2(__uint_as_float(r[x + 2]) * scale, __uint_as_float(r[x + 3]) * scale);
+      w.z = pack_bf16x2(__uint_as_float(r[x + 4]) * scale, __uint_as_float(r[x + 5]) * scale);
+      w.w = pack_bf16x2(__uint_as_float(r[x + 6]) * scale, __uint_as_float(r[x + 7]) * scale);
+      d4[v] = w;
     }
   }
 }
@@ -191,7 +188,7 @@ struct ColWalk {
   }
 };
 
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(NUM_THREADS, 1)
 bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                 BwdArgs a) {
@@ -230,15 +227,15 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       mbar_init(&bar.do_empty[s], 1);
     }
     mbar_init(&bar.sdp_full, 1);
-    mbar_init(&bar.sdp_free, BM);
-    mbar_init(&bar.p_ready, BM);
+    mbar_init(&bar.sdp_free, SOFTMAX_THREADS);
+    mbar_init(&bar.p_ready, SOFTMAX_THREADS);
     mbar_init(&bar.dv_done, 1);
-    mbar_init(&bar.ds_ready, BM);
+    mbar_init(&bar.ds_ready, SOFTMAX_THREADS);
     mbar_init(&bar.dk_done, 1);
     bar.abort = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == WARP_MMA) {
     tmem_alloc(&bar.tmem_base, 512);
     tmem_relinquish();
   }
@@ -250,7 +247,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   ColWalk walk;
   walk.init(&pl, kt, hk, dm);
 
-  if (warp == 4) {
+  if (warp == WARP_PRODUCER) {
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_do);
@@ -283,7 +280,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == WARP_MMA) {
     if (lane == 0) {
       constexpr uint32_t IDESC_NT = idesc_bf16(BM, BN, 0, 0);  // S, dP
       constexpr uint32_t IDESC_TT = idesc_bf16(BN, HD, 1, 1);  // dV, dK (A, B MN-major)
@@ -344,14 +341,15 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       }
     }
   } else {
-    const int tid = threadIdx.x;
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    const uint32_t spds = base_u32 + KV_OFF_PDS;
+    const int quarter = warp & 3, half = warp >> 2;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + half * 64;
+    const uint32_t spds = base_u32 + KV_OFF_PDS + half * HALF;
     const float sl2 = dm.scale_log2;
-    const int c0 = kt * BN;
+    const int c0 = kt * BN + half * 64;
     int h, qt, cls, t = 0;
     while (walk.next(h, qt, cls)) {
-      const int i = qt * BM + tid;
+      const int i = qt * BM + row;
       const bool valid = i < S;
       const int64_t rowi = (static_cast<int64_t>(b) * dm.h_q + h) * S + i;
       float lse2 = INFINITY, dsum = 0.f;
@@ -360,27 +358,29 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         lse2 = (l == -INFINITY) ? INFINITY : l * LOG2E;
         dsum = __ldg(a.dsum + rowi);
       }
-      const bool masked = cls != LCA_TILE_FULL || c0 + BN > S || qt * BM + BM > S;
-      uint32_t bits[4] = {0u, 0u, 0u, 0u};
+      const bool masked = cls != LCA_TILE_FULL || kt * BN + BN > S || qt * BM + BM > S;
+      uint32_t bits[2] = {0u, 0u};
       if (masked && valid) {
         const RowSpan sp = row_span(a.mask, i);
-        row_tile_bits<4>(a.mask, h / dm.heads_per_map, i, c0, sp, bits);
+        row_tile_bits<2>(a.mask, h / dm.heads_per_map, i, c0, sp, bits);
       }
       mbar_wait(&bar.sdp_full, t & 1, wc);
       __syncwarp();
       tc_fence_after();
-      uint32_t pk[64], dk[64];
-      p_ds_rows<true>(lane_addr + KV_TM_S, lane_addr + KV_TM_DP, masked, bits, sl2, lse2, dsum, pk, dk);
+      uint32_t sr[64], dr[64];
+      tmem_ld64x2(lane_addr + KV_TM_S, lane_addr + KV_TM_DP, sr, dr);
       tc_fence_before();
       mbar_arrive(&bar.sdp_free);
+      uint32_t pk[32], dk[32];
+      p_ds_half<true>(sr, dr, masked, bits, sl2, lse2, dsum, pk, dk);
       if (t >= 1) mbar_wait(&bar.dk_done, (t - 1) & 1, wc);
       __syncwarp();
-      store_row_tile(spds, tid, pk);
+      store_half_row(spds, row, pk);
       fence_proxy_async_smem();
       mbar_arrive(&bar.p_ready);
       mbar_wait(&bar.dv_done, t & 1, wc);
       __syncwarp();
-      store_row_tile(spds, tid, dk);
+      store_half_row(spds, row, dk);
       fence_proxy_async_smem();
       mbar_arrive(&bar.ds_ready);
       ++t;
@@ -390,17 +390,17 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       __syncwarp();
       tc_fence_after();
     }
-    const int j = kt * BN + tid;
+    const int j = kt * BN + row;
     const bool write = j < S;
     const int64_t roff = (static_cast<int64_t>(b) * S + j) * a.k_row_stride +
-                         static_cast<int64_t>(hk) * HD;
-    store_acc_row(lane_addr + KV_TM_DV, t > 0, 1.f, a.dv + roff, write);
-    store_acc_row(lane_addr + KV_TM_DK, t > 0, dm.scale, a.dk + roff, write);
+                         static_cast<int64_t>(hk) * HD + half * 64;
+    store_acc_half(lane_addr + KV_TM_DV, t > 0, 1.f, a.dv + roff, write);
+    store_acc_half(lane_addr + KV_TM_DK, t > 0, dm.scale, a.dk + roff, write);
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == WARP_MMA) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -425,7 +425,7 @@ struct DqBars {
   int abort;
 };
 
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(NUM_THREADS, 1)
 bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
               BwdArgs a) {
@@ -459,13 +459,13 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       mbar_init(&bar.v_empty[s], 1);
     }
     mbar_init(&bar.sdp_full, 1);
-    mbar_init(&bar.sdp_free, BM);
-    mbar_init(&bar.ds_ready, BM);
+    mbar_init(&bar.sdp_free, SOFTMAX_THREADS);
+    mbar_init(&bar.ds_ready, SOFTMAX_THREADS);
     mbar_init(&bar.dq_done, 1);
     bar.abort = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == WARP_MMA) {
     tmem_alloc(&bar.tmem_base, 512);
     tmem_relinquish();
   }
@@ -475,7 +475,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   const uint32_t tmem = bar.tmem_base;
   WaitCtx wc{&bar.abort, a.err, a.timeout_ns};
 
-  if (warp == 4) {
+  if (warp == WARP_PRODUCER) {
     if (lane == 0) {
       mbar_arrive_expect_tx(&bar.qdo_full, 2 * TILE);
       for (int c = 0; c < 2; ++c) {
@@ -505,7 +505,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         }
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == WARP_MMA) {
     if (lane == 0) {
       constexpr uint32_t IDESC_NT = idesc_bf16(BM, BN, 0, 0);  // S, dP
       constexpr uint32_t IDESC_NN = idesc_bf16(BM, HD, 0, 1);  // dQ (B = K MN-major)
@@ -552,11 +552,12 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       }
     }
   } else {
-    const int tid = threadIdx.x;
-    const int i = qt * BM + tid;
+    const int quarter = warp & 3, half = warp >> 2;
+    const int row = quarter * 32 + lane;
+    const int i = qt * BM + row;
     const bool valid = i < S;
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    const uint32_t sds = base_u32 + DQ_OFF_DS;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + half * 64;
+    const uint32_t sds = base_u32 + DQ_OFF_DS + half * HALF;
     const float sl2 = dm.scale_log2;
     const int64_t rowi = (static_cast<int64_t>(b) * dm.h_q + h) * S + i;
     float lse2 = INFINITY, dsum = 0.f;
@@ -569,20 +570,21 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     for (int n = 0; n < n_tiles; ++n) {
       const int kt = __ldg(pl.kt_idx + beg + n);
       const int cls = __ldg(pl.kt_cls + beg + n);
-      const int c0 = kt * BN;
-      const bool masked = cls != LCA_TILE_FULL || c0 + BN > S || qt * BM + BM > S;
-      uint32_t bits[4] = {0u, 0u, 0u, 0u};
-      if (masked && valid) row_tile_bits<4>(a.mask, hm, i, c0, sp, bits);
+      const bool masked = cls != LCA_TILE_FULL || kt * BN + BN > S || qt * BM + BM > S;
+      uint32_t bits[2] = {0u, 0u};
+      if (masked && valid) row_tile_bits<2>(a.mask, hm, i, kt * BN + half * 64, sp, bits);
       mbar_wait(&bar.sdp_full, n & 1, wc);
       __syncwarp();
       tc_fence_after();
-      uint32_t pk[64], dk[64];
-      p_ds_rows<false>(lane_addr + DQ_TM_S, lane_addr + DQ_TM_DP, masked, bits, sl2, lse2, dsum, pk, dk);
+      uint32_t sr[64], dr[64];
+      tmem_ld64x2(lane_addr + DQ_TM_S, lane_addr + DQ_TM_DP, sr, dr);
       tc_fence_before();
       mbar_arrive(&bar.sdp_free);
+      uint32_t pk[32], dk[32];
+      p_ds_half<false>(sr, dr, masked, bits, sl2, lse2, dsum, pk, dk);
       if (n >= 1) mbar_wait(&bar.dq_done, (n - 1) & 1, wc);
       __syncwarp();
-      store_row_tile(sds, tid, dk);
+      store_half_row(sds, row, dk);
       fence_proxy_async_smem();
       mbar_arrive(&bar.ds_ready);
     }
@@ -592,13 +594,13 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       tc_fence_after();
     }
     const int64_t roff = (static_cast<int64_t>(b) * S + i) * a.o_row_stride +
-                         static_cast<int64_t>(h) * HD;
-    store_acc_row(lane_addr + DQ_TM_DQ, n_tiles > 0, dm.scale, a.dq + roff, valid);
+                         static_cast<int64_t>(h) * HD + half * 64;
+    store_acc_half(lane_addr + DQ_TM_DQ, n_tiles > 0, dm.scale, a.dq + roff, valid);
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == WARP_MMA) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -620,7 +622,7 @@ cudaError_t launch_bwd_dkdv(const CUtensorMap& tq, const CUtensorMap& tk, const 
   cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, KV_SMEM);
   if (e != cudaSuccess) return e;
-  bwd_dkdv_kernel<<<n_blocks, 192, KV_SMEM, st>>>(tq, tk, tv, tdo, a);
+  bwd_dkdv_kernel<<<n_blocks, NUM_THREADS, KV_SMEM, st>>>(tq, tk, tv, tdo, a);
   return cudaGetLastError();
 }
 
@@ -631,7 +633,7 @@ cudaError_t launch_bwd_dq(const CUtensorMap& tq, const CUtensorMap& tk, const CU
   cudaError_t e = cudaFuncSetAttribute(bwd_dq_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, DQ_SMEM);
   if (e != cudaSuccess) return e;
-  bwd_dq_kernel<<<n_blocks, 192, DQ_SMEM, st>>>(tq, tk, tv, tdo, a);
+  bwd_dq_kernel<<<n_blocks, NUM_THREADS, DQ_SMEM, st>>>(tq, tk, tv, tdo, a);
   return cudaGetLastError();
 }
 

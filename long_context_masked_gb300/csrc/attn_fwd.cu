@@ -6,14 +6,16 @@
 //
 // One CTA owns one 128-row query tile of one query head and walks that tile's list
 // of non-skipped key tiles (from the tile plan, longest lists launched first):
-//   warp 4      TMA producer: Q once, then K/V tiles into 2-stage rings;
-//   warp 5      TMEM owner and MMA issuer: S_n = Q K_n^T (tcgen05, fp32 in TMEM,
+//   warp 8      TMA producer: Q once, then K/V tiles into 2-stage rings;
+//   warp 9      TMEM owner and MMA issuer: S_n = Q K_n^T (tcgen05, fp32 in TMEM,
 //               double-buffered) and O += P_{n-1} V_{n-1} (accumulated in TMEM);
-//   warps 0-3   softmax, one query row per thread: read S_n from TMEM, apply the mask
-//               bits only on partial or ragged tiles, online softmax in fp32 with exp2,
-//               write P (bf16) into a 128-byte-swizzled shared tile for the PV MMA,
-//               rescale the O accumulator in TMEM when the running max moves by more
-//               than 2^8 (exact after the final 1/l normalisation), then the epilogue.
+//   warps 0-7   softmax, two threads per query row (warps w and w+4 share TMEM lanes
+//               and take key columns 0-63 / 64-127): read S_n from TMEM, apply the mask
+//               bits only on partial or ragged tiles, combine the two halves' row
+//               maxima through shared memory, online softmax in fp32 with exp2, write P
+//               (bf16) into a 128-byte-swizzled shared tile for the PV MMA, rescale the
+//               O accumulator in TMEM when the running max moves by more than 2^8
+//               (exact after the final 1/l normalisation), then the epilogue.
 // Tile = 128 x 128, head_dim = 128.  All waits are bounded.
 #include <cuda_runtime.h>
 
@@ -31,13 +33,19 @@ constexpr uint32_t TILE_BYTES = BM * HD * 2;   // 32 KB, two 128-byte-swizzled h
 constexpr uint32_t HALF_BYTES = TILE_BYTES / 2;
 constexpr float RESCALE_THRESHOLD = 8.0f;      // log2 units
 
+constexpr int NUM_THREADS = 320;     // 8 softmax warps, producer, MMA issuer
+constexpr int SOFTMAX_THREADS = 256;
+constexpr int WARP_PRODUCER = 8, WARP_MMA = 9;
+constexpr int BAR_SOFTMAX = 1;        // named barrier of the softmax warps
+
 // shared memory map (offsets from a 1024-aligned base)
 constexpr uint32_t OFF_Q = 0;
 constexpr uint32_t OFF_K = OFF_Q + TILE_BYTES;        // 2 stages
 constexpr uint32_t OFF_V = OFF_K + 2 * TILE_BYTES;    // 2 stages
-constexpr uint32_t OFF_P = OFF_V + 2 * TILE_BYTES;    // 2 buffers
-constexpr uint32_t OFF_BAR = OFF_P + 2 * TILE_BYTES;
-constexpr uint32_t SMEM_BYTES = OFF_BAR + 256 + 1024;  // + barriers + alignment slack
+constexpr uint32_t OFF_P = OFF_V + 2 * TILE_BYTES;    // 1 buffer
+constexpr uint32_t OFF_BAR = OFF_P + TILE_BYTES;
+constexpr uint32_t OFF_RED = OFF_BAR + 256;           // row-max / row-sum exchange
+constexpr uint32_t SMEM_BYTES = OFF_RED + 2 * 2 * BM * 4 + 1024;  // + alignment slack
 
 // TMEM columns
 constexpr uint32_t TM_S0 = 0, TM_O = 256, TM_COLS = 512;
@@ -58,7 +66,7 @@ __device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile, int kk) {
   return desc_mnmajor(tile, kk, HALF_BYTES);
 }
 
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(NUM_THREADS, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, FwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -95,13 +103,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       mbar_init(&bar.v_full[s], 1);
       mbar_init(&bar.v_empty[s], 1);
       mbar_init(&bar.s_full[s], 1);
-      mbar_init(&bar.p_ready[s], BM);
+      mbar_init(&bar.p_ready[s], SOFTMAX_THREADS);
       mbar_init(&bar.pv_done[s], 1);
     }
     bar.abort = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == WARP_MMA) {
     tmem_alloc(&bar.tmem_base, TM_COLS);
     tmem_relinquish();
   }
@@ -111,7 +119,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   const uint32_t tmem = bar.tmem_base;
   WaitCtx wc{&bar.abort, a.err, a.timeout_ns};
 
-  if (warp == 4) {
+  if (warp == WARP_PRODUCER) {
     // ------------------------------------------------ TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
@@ -143,7 +151,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == WARP_MMA) {
     // ------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t IDESC_QK = idesc_bf16(BM, BN, 0, 0);
@@ -155,7 +163,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         mbar_wait(&bar.p_ready[st], ph, wc);
         mbar_wait(&bar.v_full[st], ph, wc);
         tc_fence_after();
-        const uint32_t sp = base_u32 + OFF_P + st * TILE_BYTES;
+        const uint32_t sp = base_u32 + OFF_P;
         const uint32_t sv = base_u32 + OFF_V + st * TILE_BYTES;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
@@ -183,94 +191,94 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       if (n_tiles >= 1) issue_pv(n_tiles - 1);
     }
   } else {
-    // ------------------------------------------------ softmax warps 0-3
-    const int t = threadIdx.x;  // row within the tile = TMEM lane
+    // ------------------------------------------------ softmax warps 0-7
+    const int quarter = warp & 3;          // TMEM lane quarter
+    const int half = warp >> 2;            // key columns [64 * half, 64 * half + 64)
+    const int t = quarter * 32 + lane;     // row within the tile = TMEM lane
     const int i = qt * BM + t;
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + half * 64;
     const RowSpan sp = row_span(a.mask, min(i, S - 1));
     const float sl2 = dm.scale_log2;
+    float* red = reinterpret_cast<float*>(base + OFF_RED);  // [parity][half][row]
     float m_run = -INFINITY;
     float l_run = 0.f;
-    uint8_t* sP = base + OFF_P;
+    const uint32_t p_tile = base_u32 + OFF_P + half * HALF_BYTES;
 
     for (int n = 0; n < n_tiles; ++n) {
       const int st = n & 1;
       const uint32_t ph = (n >> 1) & 1;
       const int kt = __ldg(pl.kt_idx + beg + n);
       const int cls = __ldg(pl.kt_cls + beg + n);
+      const int c0 = kt * BN + half * 64;
+      const bool masked = cls != LCA_TILE_FULL || kt * BN + BN > S;
+      uint32_t bits[2] = {0u, 0u};
+      if (masked && i < S) row_tile_bits<2>(a.mask, hm, i, c0, sp, bits);
       mbar_wait(&bar.s_full[st], ph, wc);
       __syncwarp();
       tc_fence_after();
-      float s[BN];
+      uint32_t r[64];
+      tmem_ld64(lane_addr + TM_S0 + st * BN, r);
+      float s[64];
 #pragma unroll
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(lane_addr + TM_S0 + st * BN + c * 32, r);
+      for (int x = 0; x < 64; ++x) s[x] = __uint_as_float(r[x]);
+      if (masked) {
 #pragma unroll
-        for (int x = 0; x < 32; ++x) s[c * 32 + x] = __uint_as_float(r[x]);
-      }
-      const int c0 = kt * BN;
-      if (cls != LCA_TILE_FULL || c0 + BN > S) {
-        uint32_t bits[BN / 32];
-        if (i < S) {
-          row_tile_bits<BN / 32>(a.mask, hm, i, c0, sp, bits);
-        } else {
-#pragma unroll
-          for (int w = 0; w < BN / 32; ++w) bits[w] = 0u;
-        }
-#pragma unroll
-        for (int x = 0; x < BN; ++x)
+        for (int x = 0; x < 64; ++x)
           if (!((bits[x >> 5] >> (x & 31)) & 1u)) s[x] = -INFINITY;
       }
-      float mx = s[0];
+      float mq[8];
 #pragma unroll
-      for (int x = 1; x < BN; ++x) mx = fmaxf(mx, s[x]);
+      for (int k = 0; k < 8; ++k) mq[k] = s[k];
+#pragma unroll
+      for (int x = 8; x < 64; x += 8)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mq[k] = fmaxf(mq[k], s[x + k]);
+      float mx = fmaxf(fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])),
+                       fmaxf(fmaxf(mq[4], mq[5]), fmaxf(mq[6], mq[7])));
+      red[(st * 2 + half) * BM + t] = mx;
+      named_bar_sync(BAR_SOFTMAX, SOFTMAX_THREADS);
+      mx = fmaxf(mx, red[(st * 2 + (half ^ 1)) * BM + t]);
       const float mt = mx * sl2;
       float alpha = 1.f;
       bool rescale = false;
       if (mt > m_run + RESCALE_THRESHOLD) {
-        rescale = (l_run > 0.f);
+        rescale = (m_run != -INFINITY);
         alpha = ex2_approx(m_run - mt);
         l_run *= alpha;
         m_run = mt;
       }
       if (__any_sync(0xFFFFFFFFu, rescale)) {
-        // O holds P_0..P_{n-1} V: wait for the last PV, scale the row, store back
+        // O holds P_0..P_{n-1} V: wait for the last PV, scale this half row, store back
         const int pj = n - 1;
         mbar_wait(&bar.pv_done[pj & 1], (pj >> 1) & 1, wc);
         __syncwarp();
         tc_fence_after();
         const float f = rescale ? alpha : 1.f;
+        uint32_t o[64];
+        tmem_ld64(lane_addr + TM_O, o);
 #pragma unroll
-        for (int c = 0; c < HD / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld32(lane_addr + TM_O + c * 32, r);
-#pragma unroll
-          for (int x = 0; x < 32; ++x) r[x] = __float_as_uint(__uint_as_float(r[x]) * f);
-          tmem_st32(lane_addr + TM_O + c * 32, r);
-        }
+        for (int x = 0; x < 64; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * f);
+        tmem_st64(lane_addr + TM_O, o);
       }
       const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-      float lsum = 0.f;
+      float ls[8];
 #pragma unroll
-      for (int x = 0; x < BN; ++x) {
+      for (int k = 0; k < 8; ++k) ls[k] = 0.f;
+#pragma unroll
+      for (int x = 0; x < 64; ++x) {
         s[x] = ex2_approx(fmaf(s[x], sl2, -m_use));
-        lsum += s[x];
+        ls[x & 7] += s[x];
       }
-      l_run += lsum;
-      // P buffer st is free once PV_{n-2} completed
-      if (n >= 2) mbar_wait(&bar.pv_done[st], ph ^ 1u, wc);
+      l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+      // the P tile is free once PV_{n-1} completed
+      if (n >= 1) mbar_wait(&bar.pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1, wc);
       __syncwarp();
-      const uint32_t p_tile = smem_u32(sP + st * TILE_BYTES);
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int x = hh * 64 + u * 8;
-          st_shared_v4(p_tile + hh * HALF_BYTES + sw128_offset(t, u),
-                       pack_bf16x2(s[x + 0], s[x + 1]), pack_bf16x2(s[x + 2], s[x + 3]),
-                       pack_bf16x2(s[x + 4], s[x + 5]), pack_bf16x2(s[x + 6], s[x + 7]));
-        }
+      for (int u = 0; u < 8; ++u) {
+        const int x = u * 8;
+        st_shared_v4(p_tile + sw128_offset(t, u), pack_bf16x2(s[x + 0], s[x + 1]),
+                     pack_bf16x2(s[x + 2], s[x + 3]), pack_bf16x2(s[x + 4], s[x + 5]),
+                     pack_bf16x2(s[x + 6], s[x + 7]));
       }
       fence_proxy_async_smem();
       tc_fence_before();
@@ -284,42 +292,45 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       __syncwarp();
       tc_fence_after();
     }
-    const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
-    __nv_bfloat16* orow = a.o + (static_cast<int64_t>(b) * S + i) * a.o_row_stride +
-                          static_cast<int64_t>(h) * HD;
+    // row-sum exchange in the slots of parity n_tiles & 1: last written for tile
+    // n_tiles - 2, whose reads both threads finished before the last tile's barrier
+    const int pe = n_tiles & 1;
+    red[(pe * 2 + half) * BM + t] = l_run;
+    named_bar_sync(BAR_SOFTMAX, SOFTMAX_THREADS);
+    const float l_tot = l_run + red[(pe * 2 + (half ^ 1)) * BM + t];
+    const float inv = (l_tot > 0.f) ? 1.f / l_tot : 0.f;
+    uint32_t o[64];
+    if (n_tiles > 0) {
+      tmem_ld64(lane_addr + TM_O, o);
+    } else {
 #pragma unroll
-    for (int c = 0; c < HD / 32; ++c) {
-      uint32_t r[32];
-      if (n_tiles > 0) {
-        tmem_ld32(lane_addr + TM_O + c * 32, r);
-      } else {
-#pragma unroll
-        for (int x = 0; x < 32; ++x) r[x] = 0u;
-      }
-      if (i < S) {
-        uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-#pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          const int x = v * 8;
-          uint4 w;
-          w.x = pack_bf16x2(__uint_as_float(r[x + 0]) * inv, __uint_as_float(r[x + 1]) * inv);
-          w.y = pack_bf16x2(__uint_as_float(r[x + 2]) * inv, __uint_as_float(r[x + 3]) * inv);
-          w.z = pack_bf16x2(__uint_as_float(r[x + 4]) * inv, __uint_as_float(r[x + 5]) * inv);
-          w.w = pack_bf16x2(__uint_as_float(r[x + 6]) * inv, __uint_as_float(r[x + 7]) * inv);
-          dst[v] = w;
-        }
-      }
+      for (int x = 0; x < 64; ++x) o[x] = 0u;
     }
     if (i < S) {
-      const float lse = (l_run > 0.f) ? (m_run + __log2f(l_run)) * 0.69314718055994531f
-                                      : -INFINITY;
-      a.lse[(static_cast<int64_t>(b) * dm.h_q + h) * S + i] = lse;
+      __nv_bfloat16* orow = a.o + (static_cast<int64_t>(b) * S + i) * a.o_row_stride +
+                            static_cast<int64_t>(h) * HD + half * 64;
+      uint4* dst = reinterpret_cast<uint4*>(orow);
+#pragma unroll
+      for (int v = 0; v < 8; ++v) {
+        const int x = v * 8;
+        uint4 w;
+        w.x = pack_bf16x2(__uint_as_float(o[x + 0]) * inv, __uint_as_float(o[x + 1]) * inv);
+        w.y = pack_bf16x2(__uint_as_float(o[x + 2]) * inv, __uint_as_float(o[x + 3]) * inv);
+        w.z = pack_bf16x2(__uint_as_float(o[x + 4]) * inv, __uint_as_float(o[x + 5]) * inv);
+        w.w = pack_bf16x2(__uint_as_float(o[x + 6]) * inv, __uint_as_float(o[x + 7]) * inv);
+        dst[v] = w;
+      }
+      if (half == 0) {
+        const float lse = (l_tot > 0.f) ? (m_run + __log2f(l_tot)) * 0.69314718055994531f
+                                        : -INFINITY;
+        a.lse[(static_cast<int64_t>(b) * dm.h_q + h) * S + i] = lse;
+      }
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == WARP_MMA) {
     tc_fence_after();
     tmem_dealloc(tmem, TM_COLS);
   }
@@ -335,7 +346,7 @@ cudaError_t launch_attn_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const 
   cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  attn_fwd_kernel<<<n_blocks, 192, SMEM_BYTES, st>>>(tq, tk, tv, args);
+  attn_fwd_kernel<<<n_blocks, NUM_THREADS, SMEM_BYTES, st>>>(tq, tk, tv, args);
   return cudaGetLastError();
 }
 

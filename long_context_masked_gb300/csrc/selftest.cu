@@ -31,6 +31,8 @@ constexpr uint32_t T_HALF = T_BYTES / 2;
 // variant 1: C = A B,   A K-major via TMA, B MN-major via TMA
 // variant 2: C = A B,   A K-major written by threads (swizzled stores), B MN-major via TMA
 // variant 3: C = A B,   A MN-major via TMA (memory holds A^T), B MN-major via TMA
+// variant 4: C = A B,   A in TMEM (rows written by the threads as bf16 pairs with
+//                       tcgen05.st), B MN-major via TMA
 __global__ void __launch_bounds__(128, 1)
 selftest_umma_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb,
                      const __nv_bfloat16* a_rm, float* c, int variant, unsigned int* err) {
@@ -51,7 +53,7 @@ selftest_umma_kernel(const __grid_constant__ CUtensorMap ta, const __grid_consta
     fence_mbar_init();
   }
   if (warp == 0) {
-    tmem_alloc(tslot, 128);
+    tmem_alloc(tslot, 256);   // D: columns 0-127; A (variant 4): columns 128-191
     tmem_relinquish();
   }
   if (variant == 2) {
@@ -68,12 +70,21 @@ selftest_umma_kernel(const __grid_constant__ CUtensorMap ta, const __grid_consta
   tc_fence_after();
   const uint32_t tmem = *tslot;
   WaitCtx wc{abort_flag, err, 2000000000ull};
+  if (variant == 4) {
+    uint32_t r[64];
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(a_rm + t * 128);
+    for (int x = 0; x < 64; ++x) r[x] = src[x];
+    tmem_st64(tmem + (static_cast<uint32_t>(warp * 32) << 16) + 128, r);
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
 
   if (t == 0) {
-    const uint32_t bytes = (variant == 2 ? 1u : 2u) * T_BYTES;
+    const uint32_t bytes = (variant == 2 || variant == 4 ? 1u : 2u) * T_BYTES;
     mbar_arrive_expect_tx(full, bytes);
     for (int hh = 0; hh < 2; ++hh) {
-      if (variant != 2) tma_load_4d(base + hh * T_HALF, &ta, full, hh * 64, 0, 0, 0);
+      if (variant != 2 && variant != 4) tma_load_4d(base + hh * T_HALF, &ta, full, hh * 64, 0, 0, 0);
       tma_load_4d(base + T_BYTES + hh * T_HALF, &tb, full, hh * 64, 0, 0, 0);
     }
     mbar_wait(full, 0, wc);
@@ -85,7 +96,10 @@ selftest_umma_kernel(const __grid_constant__ CUtensorMap ta, const __grid_consta
       const uint64_t ad = a_mn ? desc_mnmajor(base_u32, kk, T_HALF) : desc_kmajor(base_u32, kk, T_HALF);
       const uint64_t bd = b_mn ? desc_mnmajor(base_u32 + T_BYTES, kk, T_HALF)
                                : desc_kmajor(base_u32 + T_BYTES, kk, T_HALF);
-      umma_bf16_ss(tmem, ad, bd, idesc, kk > 0 ? 1u : 0u);
+      if (variant == 4)
+        umma_bf16_ts(tmem, tmem + 128 + kk * 8, bd, idesc, kk > 0 ? 1u : 0u);
+      else
+        umma_bf16_ss(tmem, ad, bd, idesc, kk > 0 ? 1u : 0u);
     }
     umma_commit(done);
   }
@@ -103,7 +117,7 @@ selftest_umma_kernel(const __grid_constant__ CUtensorMap ta, const __grid_consta
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, 128);
+    tmem_dealloc(tmem, 256);
   }
 }
 
