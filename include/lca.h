@@ -204,8 +204,9 @@ lca_status lca_attn_bwd_noalloc(const lca_plan* plan, const lca_shape* shape, co
                                 const float* lse, void* dq, void* dk, void* dv,
                                 float softmax_scale, void* stream);
 
-/* Synchronise `stream`, read and clear the device error word: LCA_OK, or
- * LCA_ERR_TIMEOUT when a bounded device wait ran out since the last call. */
+/* Synchronise `stream`, read and clear the device error word: LCA_OK, LCA_ERR_TIMEOUT
+ * when a bounded device wait ran out since the last call, or LCA_ERR_CUDA when a kernel
+ * refused to run (its shared memory came up without the alignment it needs). */
 lca_status lca_get_last_device_error(void* stream);
 
 /* Bound, in nanoseconds, of every device-side wait of later launches (default 2 s). */

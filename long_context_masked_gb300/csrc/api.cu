@@ -520,7 +520,8 @@ lca_status lca_get_last_device_error(void* stream) {
   if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(v)) != cudaSuccess) return LCA_ERR_CUDA;
   const unsigned int zero = 0;
   if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(zero)) != cudaSuccess) return LCA_ERR_CUDA;
-  return (v & LCA_DEVERR_TIMEOUT) ? LCA_ERR_TIMEOUT : LCA_OK;
+  if (v & LCA_DEVERR_TIMEOUT) return LCA_ERR_TIMEOUT;
+  return v ? LCA_ERR_CUDA : LCA_OK;
 }
 
 lca_status lca_selftest_wait_timeout(uint64_t timeout_ns, void* stream) {

@@ -12,7 +12,8 @@
 //               the KV group, recomputing S and dP with tcgen05 and accumulating dV and
 //               dK in TMEM;
 //   dQ          one CTA per (query head, query tile): loops over the tile's key tiles,
-//               recomputing S, dP and dS and accumulating dQ in TMEM.
+//               recomputing S, dP and dS and accumulating dQ in TMEM; dS goes to TMEM
+//               (bf16 pairs) and feeds the dQ MMA from there.
 // Warp roles as in the forward: warp 8 issues TMA loads, warp 9 owns TMEM and issues
 // the MMAs, warps 0-7 (two threads per query row, 64 key columns each) load their
 // halves of S and dP from TMEM behind one wait - which frees both accumulators at once,
@@ -71,9 +72,10 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(BwdArgs a) {
 
 // ------------------------------------------------------------------ shared pieces
 
-constexpr int NUM_THREADS = 320;     // 8 softmax warps, producer, MMA issuer
+constexpr int KV_THREADS = 320;      // dK/dV: 8 softmax warps, producer, MMA issuer
+constexpr int DQ_THREADS = 352;      // dQ: the same plus a second producer warp
 constexpr int SOFTMAX_THREADS = 256;
-constexpr int WARP_PRODUCER = 8, WARP_MMA = 9;
+constexpr int WARP_PRODUCER = 8, WARP_MMA = 9, WARP_PRODUCER_2 = 10;
 
 // Half a row (64 key columns) of P = exp2(s * scale_log2 - lse_log2) on allowed
 // entries and dS = P (dP - D), packed to bf16 pairs (P only when WANT_P).
@@ -147,6 +149,7 @@ constexpr uint32_t KV_OFF_DO = 4 * TILE;       // 2 stages
 constexpr uint32_t KV_OFF_PDS = 6 * TILE;
 constexpr uint32_t KV_OFF_BAR = 7 * TILE;
 constexpr uint32_t KV_SMEM = KV_OFF_BAR + 256 + 1024;
+static_assert(KV_SMEM <= 232448, "dynamic shared memory above the 227 KB per-CTA limit");
 constexpr uint32_t KV_TM_S = 0, KV_TM_DP = 128, KV_TM_DV = 256, KV_TM_DK = 384;
 
 struct KvBars {
@@ -188,7 +191,7 @@ struct ColWalk {
   }
 };
 
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(KV_THREADS, 1)
 bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                 BwdArgs a) {
@@ -284,8 +287,13 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if (lane == 0) {
       constexpr uint32_t IDESC_NT = idesc_bf16(BM, BN, 0, 0);  // S, dP
       constexpr uint32_t IDESC_TT = idesc_bf16(BN, HD, 1, 1);  // dV, dK (A, B MN-major)
-      const uint32_t sk = base_u32 + KV_OFF_K, sv = base_u32 + KV_OFF_V;
-      const uint32_t spds = base_u32 + KV_OFF_PDS;
+      const uint64_t dk_ = desc_kmajor(base_u32 + KV_OFF_K, 0, HALF);
+      const uint64_t dv_ = desc_kmajor(base_u32 + KV_OFF_V, 0, HALF);
+      const uint64_t dq_k0 = desc_kmajor(base_u32 + KV_OFF_Q, 0, HALF);
+      const uint64_t ddo_k0 = desc_kmajor(base_u32 + KV_OFF_DO, 0, HALF);
+      const uint64_t dq_m0 = desc_mnmajor(base_u32 + KV_OFF_Q, 0, HALF);
+      const uint64_t ddo_m0 = desc_mnmajor(base_u32 + KV_OFF_DO, 0, HALF);
+      const uint64_t dpds = desc_mnmajor(base_u32 + KV_OFF_PDS, 0, HALF);
       int total = 0;
       {
         ColWalk w2 = walk;
@@ -295,19 +303,19 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       auto issue_sdp = [&](int t) {
         const int st = t & 1;
         const uint32_t ph = (t >> 1) & 1;
-        const uint32_t sq = base_u32 + KV_OFF_Q + st * TILE;
-        const uint32_t sdo = base_u32 + KV_OFF_DO + st * TILE;
+        const uint64_t dq = dq_k0 + st * stage_step(TILE);
+        const uint64_t ddo = ddo_k0 + st * stage_step(TILE);
         mbar_wait(&bar.q_full[st], ph, wc);
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk)
-          umma_bf16_ss(tmem + KV_TM_S, desc_kmajor(sq, kk, HALF), desc_kmajor(sk, kk, HALF),
+          umma_bf16_ss(tmem + KV_TM_S, dq + kmajor_step(kk, HALF), dk_ + kmajor_step(kk, HALF),
                        IDESC_NT, kk > 0 ? 1u : 0u);
         mbar_wait(&bar.do_full[st], ph, wc);
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk)
-          umma_bf16_ss(tmem + KV_TM_DP, desc_kmajor(sdo, kk, HALF), desc_kmajor(sv, kk, HALF),
+          umma_bf16_ss(tmem + KV_TM_DP, ddo + kmajor_step(kk, HALF), dv_ + kmajor_step(kk, HALF),
                        IDESC_NT, kk > 0 ? 1u : 0u);
         umma_commit(&bar.sdp_full);
       };
@@ -320,13 +328,13 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           mbar_wait(&bar.sdp_free, par, wc);
           issue_sdp(t + 1);
         }
-        const uint32_t sq = base_u32 + KV_OFF_Q + st * TILE;
-        const uint32_t sdo = base_u32 + KV_OFF_DO + st * TILE;
+        const uint64_t dq = dq_m0 + st * stage_step(TILE);
+        const uint64_t ddo = ddo_m0 + st * stage_step(TILE);
         mbar_wait(&bar.p_ready, par, wc);
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BM / 16; ++kk)
-          umma_bf16_ss(tmem + KV_TM_DV, desc_mnmajor(spds, kk, HALF), desc_mnmajor(sdo, kk, HALF),
+          umma_bf16_ss(tmem + KV_TM_DV, dpds + mnmajor_step(kk), ddo + mnmajor_step(kk),
                        IDESC_TT, (t > 0 || kk > 0) ? 1u : 0u);
         umma_commit(&bar.dv_done);
         umma_commit(&bar.do_empty[st]);
@@ -334,7 +342,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BM / 16; ++kk)
-          umma_bf16_ss(tmem + KV_TM_DK, desc_mnmajor(spds, kk, HALF), desc_mnmajor(sq, kk, HALF),
+          umma_bf16_ss(tmem + KV_TM_DK, dpds + mnmajor_step(kk), dq + mnmajor_step(kk),
                        IDESC_TT, (t > 0 || kk > 0) ? 1u : 0u);
         umma_commit(&bar.dk_done);
         umma_commit(&bar.q_empty[st]);
@@ -412,10 +420,10 @@ constexpr uint32_t DQ_OFF_Q = 0;
 constexpr uint32_t DQ_OFF_DO = TILE;
 constexpr uint32_t DQ_OFF_K = 2 * TILE;        // 2 stages
 constexpr uint32_t DQ_OFF_V = 4 * TILE;        // 2 stages
-constexpr uint32_t DQ_OFF_DS = 6 * TILE;
-constexpr uint32_t DQ_OFF_BAR = 7 * TILE;
+constexpr uint32_t DQ_OFF_BAR = 6 * TILE;
 constexpr uint32_t DQ_SMEM = DQ_OFF_BAR + 256 + 1024;
-constexpr uint32_t DQ_TM_S = 0, DQ_TM_DP = 128, DQ_TM_DQ = 256;
+static_assert(DQ_SMEM <= 232448, "dynamic shared memory above the 227 KB per-CTA limit");
+constexpr uint32_t DQ_TM_S = 0, DQ_TM_DP = 128, DQ_TM_DQ = 256, DQ_TM_DS = 384;
 
 struct DqBars {
   uint64_t qdo_full;
@@ -425,7 +433,7 @@ struct DqBars {
   int abort;
 };
 
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(DQ_THREADS, 1)
 bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
               BwdArgs a) {
@@ -491,6 +499,21 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         for (int c = 0; c < 2; ++c)
           tma_load_4d(base + DQ_OFF_K + st * TILE + c * HALF, &tm_k, &bar.k_full[st], c * 64, hk,
                       kt * BN, b);
+      }
+      if (bar.abort) {
+        mbar_wait_final(&bar.qdo_full, 0, a.timeout_ns);
+        for (int n = max(0, n_tiles - 2); n < n_tiles; ++n)
+          mbar_wait_final(&bar.k_full[n & 1], (n >> 1) & 1, a.timeout_ns);
+      }
+    }
+  } else if (warp == WARP_PRODUCER_2) {
+    if (lane == 0) {
+      // V stages are released after dP, earlier than K stages (released after dQ):
+      // a separate warp keeps V loads from queueing behind K releases
+      for (int n = 0; n < n_tiles; ++n) {
+        const int kt = __ldg(pl.kt_idx + beg + n);
+        const int st = n & 1;
+        const uint32_t ph = (n >> 1) & 1;
         if (n >= 2) mbar_wait(&bar.v_empty[st], ph ^ 1u, wc);
         mbar_arrive_expect_tx(&bar.v_full[st], TILE);
         for (int c = 0; c < 2; ++c)
@@ -498,35 +521,35 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                       kt * BN, b);
       }
       if (bar.abort) {
-        mbar_wait_final(&bar.qdo_full, 0, a.timeout_ns);
-        for (int n = max(0, n_tiles - 2); n < n_tiles; ++n) {
-          mbar_wait_final(&bar.k_full[n & 1], (n >> 1) & 1, a.timeout_ns);
+        for (int n = max(0, n_tiles - 2); n < n_tiles; ++n)
           mbar_wait_final(&bar.v_full[n & 1], (n >> 1) & 1, a.timeout_ns);
-        }
       }
     }
   } else if (warp == WARP_MMA) {
     if (lane == 0) {
       constexpr uint32_t IDESC_NT = idesc_bf16(BM, BN, 0, 0);  // S, dP
       constexpr uint32_t IDESC_NN = idesc_bf16(BM, HD, 0, 1);  // dQ (B = K MN-major)
-      const uint32_t sq = base_u32 + DQ_OFF_Q, sdo = base_u32 + DQ_OFF_DO;
-      const uint32_t sds = base_u32 + DQ_OFF_DS;
+      const uint64_t dq_ = desc_kmajor(base_u32 + DQ_OFF_Q, 0, HALF);
+      const uint64_t ddo_ = desc_kmajor(base_u32 + DQ_OFF_DO, 0, HALF);
+      const uint64_t dk_k0 = desc_kmajor(base_u32 + DQ_OFF_K, 0, HALF);
+      const uint64_t dk_m0 = desc_mnmajor(base_u32 + DQ_OFF_K, 0, HALF);
+      const uint64_t dv_k0 = desc_kmajor(base_u32 + DQ_OFF_V, 0, HALF);
       auto issue_sdp = [&](int n) {
         const int st = n & 1;
         const uint32_t ph = (n >> 1) & 1;
-        const uint32_t sk = base_u32 + DQ_OFF_K + st * TILE;
-        const uint32_t sv = base_u32 + DQ_OFF_V + st * TILE;
+        const uint64_t dk = dk_k0 + st * stage_step(TILE);
+        const uint64_t dv = dv_k0 + st * stage_step(TILE);
         mbar_wait(&bar.k_full[st], ph, wc);
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk)
-          umma_bf16_ss(tmem + DQ_TM_S, desc_kmajor(sq, kk, HALF), desc_kmajor(sk, kk, HALF),
+          umma_bf16_ss(tmem + DQ_TM_S, dq_ + kmajor_step(kk, HALF), dk + kmajor_step(kk, HALF),
                        IDESC_NT, kk > 0 ? 1u : 0u);
         mbar_wait(&bar.v_full[st], ph, wc);
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk)
-          umma_bf16_ss(tmem + DQ_TM_DP, desc_kmajor(sdo, kk, HALF), desc_kmajor(sv, kk, HALF),
+          umma_bf16_ss(tmem + DQ_TM_DP, ddo_ + kmajor_step(kk, HALF), dv + kmajor_step(kk, HALF),
                        IDESC_NT, kk > 0 ? 1u : 0u);
         umma_commit(&bar.sdp_full);
         umma_commit(&bar.v_empty[st]);
@@ -540,12 +563,12 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           mbar_wait(&bar.sdp_free, par, wc);
           issue_sdp(n + 1);
         }
-        const uint32_t sk = base_u32 + DQ_OFF_K + st * TILE;
+        const uint64_t dk = dk_m0 + st * stage_step(TILE);
         mbar_wait(&bar.ds_ready, par, wc);
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          umma_bf16_ss(tmem + DQ_TM_DQ, desc_kmajor(sds, kk, HALF), desc_mnmajor(sk, kk, HALF),
+          umma_bf16_ts(tmem + DQ_TM_DQ, tmem + DQ_TM_DS + kk * 8, dk + mnmajor_step(kk),
                        IDESC_NN, (n > 0 || kk > 0) ? 1u : 0u);
         umma_commit(&bar.dq_done);
         umma_commit(&bar.k_empty[st]);
@@ -556,8 +579,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     const int row = quarter * 32 + lane;
     const int i = qt * BM + row;
     const bool valid = i < S;
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + half * 64;
-    const uint32_t sds = base_u32 + DQ_OFF_DS + half * HALF;
+    const uint32_t quarter_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t lane_addr = quarter_addr + half * 64;
     const float sl2 = dm.scale_log2;
     const int64_t rowi = (static_cast<int64_t>(b) * dm.h_q + h) * S + i;
     float lse2 = INFINITY, dsum = 0.f;
@@ -582,10 +605,11 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       mbar_arrive(&bar.sdp_free);
       uint32_t pk[32], dk[32];
       p_ds_half<false>(sr, dr, masked, bits, sl2, lse2, dsum, pk, dk);
-      if (n >= 1) mbar_wait(&bar.dq_done, (n - 1) & 1, wc);
+      if (n >= 1) mbar_wait(&bar.dq_done, (n - 1) & 1, wc);   // dQ_{n-1} read dS_{n-1}
       __syncwarp();
-      store_half_row(sds, row, dk);
-      fence_proxy_async_smem();
+      tc_fence_after();
+      tmem_st32(quarter_addr + DQ_TM_DS + half * 32, dk);
+      tc_fence_before();
       mbar_arrive(&bar.ds_ready);
     }
     if (n_tiles > 0) {
@@ -622,7 +646,7 @@ cudaError_t launch_bwd_dkdv(const CUtensorMap& tq, const CUtensorMap& tk, const 
   cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, KV_SMEM);
   if (e != cudaSuccess) return e;
-  bwd_dkdv_kernel<<<n_blocks, NUM_THREADS, KV_SMEM, st>>>(tq, tk, tv, tdo, a);
+  bwd_dkdv_kernel<<<n_blocks, KV_THREADS, KV_SMEM, st>>>(tq, tk, tv, tdo, a);
   return cudaGetLastError();
 }
 
@@ -633,7 +657,7 @@ cudaError_t launch_bwd_dq(const CUtensorMap& tq, const CUtensorMap& tk, const CU
   cudaError_t e = cudaFuncSetAttribute(bwd_dq_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, DQ_SMEM);
   if (e != cudaSuccess) return e;
-  bwd_dq_kernel<<<n_blocks, NUM_THREADS, DQ_SMEM, st>>>(tq, tk, tv, tdo, a);
+  bwd_dq_kernel<<<n_blocks, DQ_THREADS, DQ_SMEM, st>>>(tq, tk, tv, tdo, a);
   return cudaGetLastError();
 }
 

@@ -6,16 +6,21 @@
 //
 // One CTA owns one 128-row query tile of one query head and walks that tile's list
 // of non-skipped key tiles (from the tile plan, longest lists launched first):
-//   warp 8      TMA producer: Q once, then K/V tiles into 2-stage rings;
-//   warp 9      TMEM owner and MMA issuer: S_n = Q K_n^T (tcgen05, fp32 in TMEM,
-//               double-buffered) and O += P_{n-1} V_{n-1} (accumulated in TMEM);
+//   warps 8, 10 TMA producers: Q once and the K tiles (warp 8), the V tiles (warp 10),
+//               each into a 3-stage ring;
+//   warp 9      TMEM owner and MMA issuer: S_n = Q K_n^T (tcgen05, both operands in
+//               shared memory, fp32 in TMEM, three buffers) and O += P_{n-2} V_{n-2}
+//               with P read from TMEM (accumulated in TMEM).  PV trails S by two
+//               tiles so that S_{n+1} is computed while the softmax works on S_n;
 //   warps 0-7   softmax, two threads per query row (warps w and w+4 share TMEM lanes
 //               and take key columns 0-63 / 64-127): read S_n from TMEM, apply the mask
 //               bits only on partial or ragged tiles, combine the two halves' row
 //               maxima through shared memory, online softmax in fp32 with exp2, write P
-//               (bf16) into a 128-byte-swizzled shared tile for the PV MMA, rescale the
-//               O accumulator in TMEM when the running max moves by more than 2^8
+//               (bf16 pairs) back into the TMEM columns of S_n for the PV MMA, rescale
+//               the O accumulator in TMEM when the running max moves by more than 2^8
 //               (exact after the final 1/l normalisation), then the epilogue.
+// Keeping P in TMEM matters on this part: an M = N = 128 MMA with both operands in
+// shared memory reads 128 B/clk, the whole shared-memory bandwidth of the SM.
 // Tile = 128 x 128, head_dim = 128.  All waits are bounded.
 #include <cuda_runtime.h>
 
@@ -33,28 +38,33 @@ constexpr uint32_t TILE_BYTES = BM * HD * 2;   // 32 KB, two 128-byte-swizzled h
 constexpr uint32_t HALF_BYTES = TILE_BYTES / 2;
 constexpr float RESCALE_THRESHOLD = 8.0f;      // log2 units
 
-constexpr int NUM_THREADS = 320;     // 8 softmax warps, producer, MMA issuer
+constexpr int NUM_THREADS = 352;     // 8 softmax warps, MMA issuer, K and V producers
 constexpr int SOFTMAX_THREADS = 256;
-constexpr int WARP_PRODUCER = 8, WARP_MMA = 9;
+constexpr int WARP_PRODUCER = 8, WARP_MMA = 9, WARP_PRODUCER_V = 10;
 constexpr int BAR_SOFTMAX = 1;        // named barrier of the softmax warps
+
+constexpr int KST = 3;                // K stages
+constexpr int VST = 3;                // V stages
+constexpr int NSB = 3;                // S buffers in TMEM
 
 // shared memory map (offsets from a 1024-aligned base)
 constexpr uint32_t OFF_Q = 0;
-constexpr uint32_t OFF_K = OFF_Q + TILE_BYTES;        // 2 stages
-constexpr uint32_t OFF_V = OFF_K + 2 * TILE_BYTES;    // 2 stages
-constexpr uint32_t OFF_P = OFF_V + 2 * TILE_BYTES;    // 1 buffer
-constexpr uint32_t OFF_BAR = OFF_P + TILE_BYTES;
+constexpr uint32_t OFF_K = OFF_Q + TILE_BYTES;          // KST stages
+constexpr uint32_t OFF_V = OFF_K + KST * TILE_BYTES;    // VST stages
+constexpr uint32_t OFF_BAR = OFF_V + VST * TILE_BYTES;
 constexpr uint32_t OFF_RED = OFF_BAR + 256;           // row-max / row-sum exchange
-constexpr uint32_t SMEM_BYTES = OFF_RED + 2 * 2 * BM * 4 + 1024;  // + alignment slack
+constexpr uint32_t SMEM_BYTES = OFF_RED + 2 * 2 * BM * 4;   // base is 1024-aligned
+static_assert(SMEM_BYTES <= 232448, "dynamic shared memory above the 227 KB per-CTA limit");
 
 // TMEM columns
-constexpr uint32_t TM_S0 = 0, TM_O = 256, TM_COLS = 512;
+constexpr uint32_t TM_S0 = 0, TM_O = NSB * BN, TM_COLS = 512;
+static_assert(TM_O + HD <= TM_COLS, "TMEM columns");
 
 struct Bars {
   uint64_t q_full;
-  uint64_t k_full[2], k_empty[2];
-  uint64_t v_full[2], v_empty[2];
-  uint64_t s_full[2], p_ready[2], pv_done[2];
+  uint64_t k_full[KST], k_empty[KST];
+  uint64_t v_full[VST], v_empty[VST];
+  uint64_t s_full[NSB], p_ready[NSB], pv_done[NSB];
   uint32_t tmem_base;
   int abort;
 };
@@ -69,10 +79,13 @@ __device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile, int kk) {
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, FwdArgs a) {
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw_u32 = smem_u32(smem_raw);
-  const uint32_t base_u32 = (raw_u32 + 1023u) & ~1023u;
-  uint8_t* base = smem_raw + (base_u32 - raw_u32);
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t base_u32 = smem_u32(smem_raw);
+  if (base_u32 & 1023u) {   // the swizzled tiles need a 1024-byte-aligned base
+    if (threadIdx.x == 0) atomicOr(a.err, LCA_DEVERR_LAYOUT);
+    return;
+  }
+  uint8_t* base = smem_raw;
   Bars& bar = *reinterpret_cast<Bars*>(base + OFF_BAR);
 
   const int warp = threadIdx.x >> 5;
@@ -97,11 +110,15 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
   if (threadIdx.x == 0) {
     mbar_init(&bar.q_full, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < KST; ++s) {
       mbar_init(&bar.k_full[s], 1);
       mbar_init(&bar.k_empty[s], 1);
+    }
+    for (int s = 0; s < VST; ++s) {
       mbar_init(&bar.v_full[s], 1);
       mbar_init(&bar.v_empty[s], 1);
+    }
+    for (int s = 0; s < NSB; ++s) {
       mbar_init(&bar.s_full[s], 1);
       mbar_init(&bar.p_ready[s], SOFTMAX_THREADS);
       mbar_init(&bar.pv_done[s], 1);
@@ -119,36 +136,44 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   const uint32_t tmem = bar.tmem_base;
   WaitCtx wc{&bar.abort, a.err, a.timeout_ns};
 
-  if (warp == WARP_PRODUCER) {
-    // ------------------------------------------------ TMA producer
-    if (lane == 0) {
+  if (warp == WARP_PRODUCER || warp == WARP_PRODUCER_V) {
+    // ------------------------------------------------ TMA producers
+    // one warp streams Q and the K tiles, another the V tiles, so a K load never
+    // queues behind the release of a V stage (V stages are freed two tiles later).
+    if (warp == WARP_PRODUCER && lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
       mbar_arrive_expect_tx(&bar.q_full, TILE_BYTES);
       for (int c = 0; c < 2; ++c)
         tma_load_4d(base + OFF_Q + c * HALF_BYTES, &tm_q, &bar.q_full, c * 64, h, qt * BM, b);
       for (int n = 0; n < n_tiles; ++n) {
         const int kt = __ldg(pl.kt_idx + beg + n);
-        const int st = n & 1;
-        const uint32_t ph = (n >> 1) & 1;
-        if (n >= 2) mbar_wait(&bar.k_empty[st], ph ^ 1u, wc);
-        mbar_arrive_expect_tx(&bar.k_full[st], TILE_BYTES);
+        const int ks = n % KST;
+        if (n >= KST) mbar_wait(&bar.k_empty[ks], (n / KST - 1) & 1, wc);
+        mbar_arrive_expect_tx(&bar.k_full[ks], TILE_BYTES);
         for (int c = 0; c < 2; ++c)
-          tma_load_4d(base + OFF_K + st * TILE_BYTES + c * HALF_BYTES, &tm_k, &bar.k_full[st],
-                      c * 64, hk, kt * BN, b);
-        if (n >= 2) mbar_wait(&bar.v_empty[st], ph ^ 1u, wc);
-        mbar_arrive_expect_tx(&bar.v_full[st], TILE_BYTES);
-        for (int c = 0; c < 2; ++c)
-          tma_load_4d(base + OFF_V + st * TILE_BYTES + c * HALF_BYTES, &tm_v, &bar.v_full[st],
+          tma_load_4d(base + OFF_K + ks * TILE_BYTES + c * HALF_BYTES, &tm_k, &bar.k_full[ks],
                       c * 64, hk, kt * BN, b);
       }
       if (bar.abort) {  // let copies in flight land before the CTA exits
         mbar_wait_final(&bar.q_full, 0, a.timeout_ns);
-        for (int n = max(0, n_tiles - 2); n < n_tiles; ++n) {
-          mbar_wait_final(&bar.k_full[n & 1], (n >> 1) & 1, a.timeout_ns);
-          mbar_wait_final(&bar.v_full[n & 1], (n >> 1) & 1, a.timeout_ns);
-        }
+        for (int n = max(0, n_tiles - KST); n < n_tiles; ++n)
+          mbar_wait_final(&bar.k_full[n % KST], (n / KST) & 1, a.timeout_ns);
+      }
+    } else if (warp == WARP_PRODUCER_V && lane == 0) {
+      tma_prefetch_desc(&tm_v);
+      for (int n = 0; n < n_tiles; ++n) {
+        const int kt = __ldg(pl.kt_idx + beg + n);
+        const int vs = n % VST;
+        if (n >= VST) mbar_wait(&bar.v_empty[vs], (n / VST - 1) & 1, wc);
+        mbar_arrive_expect_tx(&bar.v_full[vs], TILE_BYTES);
+        for (int c = 0; c < 2; ++c)
+          tma_load_4d(base + OFF_V + vs * TILE_BYTES + c * HALF_BYTES, &tm_v, &bar.v_full[vs],
+                      c * 64, hk, kt * BN, b);
+      }
+      if (bar.abort) {
+        for (int n = max(0, n_tiles - VST); n < n_tiles; ++n)
+          mbar_wait_final(&bar.v_full[n % VST], (n / VST) & 1, a.timeout_ns);
       }
     }
   } else if (warp == WARP_MMA) {
@@ -156,39 +181,45 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if (lane == 0) {
       constexpr uint32_t IDESC_QK = idesc_bf16(BM, BN, 0, 0);
       constexpr uint32_t IDESC_PV = idesc_bf16(BM, HD, 0, 1);
-      const uint32_t sq = base_u32 + OFF_Q;
+      const uint64_t dq0 = kmajor_desc(base_u32 + OFF_Q, 0);
+      const uint64_t dk0 = kmajor_desc(base_u32 + OFF_K, 0);
+      const uint64_t dv0 = mnmajor_desc(base_u32 + OFF_V, 0);
+      // P_j sits (bf16 pairs) in the first 64 TMEM columns of S buffer j % 3.  S_{j+3}
+      // reuses that buffer; it is issued after PV_j and tcgen05 MMAs of one thread run
+      // in issue order, so PV_j has read P_j before S_{j+3} overwrites it (and PV_j
+      // waited for the softmax of tile j, so S_j was consumed).
       auto issue_pv = [&](int j) {
-        const int st = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
-        mbar_wait(&bar.p_ready[st], ph, wc);
-        mbar_wait(&bar.v_full[st], ph, wc);
+        const int sb = j % NSB;
+        const int vs = j % VST;
+        mbar_wait(&bar.p_ready[sb], (j / NSB) & 1, wc);
+        mbar_wait(&bar.v_full[vs], (j / VST) & 1, wc);
         tc_fence_after();
-        const uint32_t sp = base_u32 + OFF_P;
-        const uint32_t sv = base_u32 + OFF_V + st * TILE_BYTES;
+        const uint64_t dv = dv0 + vs * stage_step(TILE_BYTES);
+        const uint32_t ta = tmem + TM_S0 + sb * BN;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          umma_bf16_ss(tmem + TM_O, kmajor_desc(sp, kk), mnmajor_desc(sv, kk), IDESC_PV,
+          umma_bf16_ts(tmem + TM_O, ta + kk * 8, dv + mnmajor_step(kk), IDESC_PV,
                        (j > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&bar.pv_done[st]);
-        umma_commit(&bar.v_empty[st]);
+        umma_commit(&bar.pv_done[sb]);
+        umma_commit(&bar.v_empty[vs]);
       };
       mbar_wait(&bar.q_full, 0, wc);
       for (int n = 0; n < n_tiles; ++n) {
-        const int st = n & 1;
-        const uint32_t ph = (n >> 1) & 1;
-        if (n >= 2) mbar_wait(&bar.p_ready[st], ph ^ 1u, wc);
-        mbar_wait(&bar.k_full[st], ph, wc);
+        const int sb = n % NSB;
+        const int ks = n % KST;
+        mbar_wait(&bar.k_full[ks], (n / KST) & 1, wc);
         tc_fence_after();
-        const uint32_t sk = base_u32 + OFF_K + st * TILE_BYTES;
+        const uint64_t dk = dk0 + ks * stage_step(TILE_BYTES);
+        const uint32_t td = tmem + TM_S0 + sb * BN;
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk)
-          umma_bf16_ss(tmem + TM_S0 + st * BN, kmajor_desc(sq, kk), kmajor_desc(sk, kk), IDESC_QK,
-                       kk > 0 ? 1u : 0u);
-        umma_commit(&bar.s_full[st]);
-        umma_commit(&bar.k_empty[st]);
-        if (n >= 1) issue_pv(n - 1);
+          umma_bf16_ss(td, dq0 + kmajor_step(kk, HALF_BYTES), dk + kmajor_step(kk, HALF_BYTES),
+                       IDESC_QK, kk > 0 ? 1u : 0u);
+        umma_commit(&bar.s_full[sb]);
+        umma_commit(&bar.k_empty[ks]);
+        if (n >= 2) issue_pv(n - 2);
       }
-      if (n_tiles >= 1) issue_pv(n_tiles - 1);
+      for (int j = max(0, n_tiles - 2); j < n_tiles; ++j) issue_pv(j);
     }
   } else {
     // ------------------------------------------------ softmax warps 0-7
@@ -196,17 +227,18 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int half = warp >> 2;            // key columns [64 * half, 64 * half + 64)
     const int t = quarter * 32 + lane;     // row within the tile = TMEM lane
     const int i = qt * BM + t;
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + half * 64;
+    const uint32_t quarter_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t lane_addr = quarter_addr + half * 64;
     const RowSpan sp = row_span(a.mask, min(i, S - 1));
     const float sl2 = dm.scale_log2;
     float* red = reinterpret_cast<float*>(base + OFF_RED);  // [parity][half][row]
     float m_run = -INFINITY;
     float l_run = 0.f;
-    const uint32_t p_tile = base_u32 + OFF_P + half * HALF_BYTES;
 
     for (int n = 0; n < n_tiles; ++n) {
-      const int st = n & 1;
-      const uint32_t ph = (n >> 1) & 1;
+      const int st = n % NSB;             // S buffer
+      const uint32_t ph = (n / NSB) & 1;
+      const int rp = n & 1;               // max-exchange parity
       const int kt = __ldg(pl.kt_idx + beg + n);
       const int cls = __ldg(pl.kt_cls + beg + n);
       const int c0 = kt * BN + half * 64;
@@ -235,9 +267,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         for (int k = 0; k < 8; ++k) mq[k] = fmaxf(mq[k], s[x + k]);
       float mx = fmaxf(fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])),
                        fmaxf(fmaxf(mq[4], mq[5]), fmaxf(mq[6], mq[7])));
-      red[(st * 2 + half) * BM + t] = mx;
+      red[(rp * 2 + half) * BM + t] = mx;
       named_bar_sync(BAR_SOFTMAX, SOFTMAX_THREADS);
-      mx = fmaxf(mx, red[(st * 2 + (half ^ 1)) * BM + t]);
+      mx = fmaxf(mx, red[(rp * 2 + (half ^ 1)) * BM + t]);
       const float mt = mx * sl2;
       float alpha = 1.f;
       bool rescale = false;
@@ -250,7 +282,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       if (__any_sync(0xFFFFFFFFu, rescale)) {
         // O holds P_0..P_{n-1} V: wait for the last PV, scale this half row, store back
         const int pj = n - 1;
-        mbar_wait(&bar.pv_done[pj & 1], (pj >> 1) & 1, wc);
+        mbar_wait(&bar.pv_done[pj % NSB], (pj / NSB) & 1, wc);
         __syncwarp();
         tc_fence_after();
         const float f = rescale ? alpha : 1.f;
@@ -270,17 +302,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         ls[x & 7] += s[x];
       }
       l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
-      // the P tile is free once PV_{n-1} completed
-      if (n >= 1) mbar_wait(&bar.pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1, wc);
-      __syncwarp();
+      // P (bf16 pairs) into the first 64 columns of this S buffer; both halves of the
+      // row finished reading S before the max exchange barrier above
+      uint32_t pk[32];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int x = u * 8;
-        st_shared_v4(p_tile + sw128_offset(t, u), pack_bf16x2(s[x + 0], s[x + 1]),
-                     pack_bf16x2(s[x + 2], s[x + 3]), pack_bf16x2(s[x + 4], s[x + 5]),
-                     pack_bf16x2(s[x + 6], s[x + 7]));
-      }
-      fence_proxy_async_smem();
+      for (int x = 0; x < 32; ++x) pk[x] = pack_bf16x2(s[2 * x], s[2 * x + 1]);
+      tmem_st32(quarter_addr + TM_S0 + st * BN + half * 32, pk);
       tc_fence_before();
       mbar_arrive(&bar.p_ready[st]);
     }
@@ -288,7 +315,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     // ---- epilogue: O = acc / l (bf16), LSE = (m + log2 l) * ln 2
     if (n_tiles > 0) {
       const int pj = n_tiles - 1;
-      mbar_wait(&bar.pv_done[pj & 1], (pj >> 1) & 1, wc);
+      mbar_wait(&bar.pv_done[pj % NSB], (pj / NSB) & 1, wc);
       __syncwarp();
       tc_fence_after();
     }

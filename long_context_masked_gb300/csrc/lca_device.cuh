@@ -175,6 +175,16 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int kk, uint32_t
   return sdesc_sw128(tile + kk * 2048, half_bytes, 1024);
 }
 
+// The same descriptors as a base (k-step 0 of stage 0) plus constant increments, so an
+// issuing thread builds each 64-bit descriptor once and steps it with an integer add:
+// the start-address field is the low 14 bits in 16-byte units and shared-memory
+// addresses stay below 2^18, so the increments never carry out of the field.
+__host__ __device__ constexpr uint64_t kmajor_step(int kk, uint32_t half_bytes) {
+  return ((kk >> 2) * half_bytes + (kk & 3) * 32) >> 4;
+}
+__host__ __device__ constexpr uint64_t mnmajor_step(int kk) { return (kk * 2048) >> 4; }
+__host__ __device__ constexpr uint64_t stage_step(uint32_t bytes) { return bytes >> 4; }
+
 // Instruction descriptor of kind::f16 with bf16 A/B and fp32 accumulation.
 // Bits: [4,6) D format (1 = f32), [7,10) A format (1 = bf16), [10,13) B format,
 // 15/16 A/B major (0 = K-major, 1 = MN-major), [17,23) N >> 3, [24,29) M >> 4.

@@ -9,6 +9,7 @@ namespace lca {
 
 // Device error word bits.
 constexpr unsigned int LCA_DEVERR_TIMEOUT = 1u;
+constexpr unsigned int LCA_DEVERR_LAYOUT = 2u;   // shared-memory base not 1024-aligned
 
 // Mask descriptor as the kernels see it (device arrays owned by the plan).
 struct MaskDev {
