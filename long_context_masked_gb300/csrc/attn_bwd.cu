@@ -72,7 +72,7 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(BwdArgs a) {
 
 // ------------------------------------------------------------------ shared pieces
 
-constexpr int KV_THREADS = 320;      // dK/dV: 8 softmax warps, producer, MMA issuer
+constexpr int KV_THREADS = 352;      // dK/dV: 8 softmax warps, producer, MMA issuer, dO producer
 constexpr int DQ_THREADS = 352;      // dQ: the same plus a second producer warp
 constexpr int SOFTMAX_THREADS = 256;
 constexpr int WARP_PRODUCER = 8, WARP_MMA = 9, WARP_PRODUCER_2 = 10;
@@ -161,7 +161,8 @@ struct KvBars {
 };
 
 // Walks the (query head, query tile) pairs feeding one key tile: every query head of
-// the KV group, each with the transposed list of its map head.
+// the KV group, each with the transposed list of its map head (head-major: measured
+// faster than query-tile-major on the GQA 64:8 workload).
 struct ColWalk {
   const PlanDev* pl;
   int kt, hk, group, heads_per_map, n_kt;
@@ -260,14 +261,42 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tma_load_4d(base + KV_OFF_V + c * HALF, &tm_v, &bar.kv_full, c * 64, hk, kt * BN, b);
       }
       int h, qt, cls, t = 0;
+      ColWalk ahead = walk;   // two steps ahead: L2 prefetch of the Q tile
+      int ha, qa, ca;
+      for (int k = 0; k < 2 && ahead.next(ha, qa, ca); ++k)
+        for (int c = 0; c < 2; ++c) tma_prefetch_l2_4d(&tm_q, c * 64, ha, qa * BM, b);
       while (walk.next(h, qt, cls)) {
         const int st = t & 1;
         const uint32_t ph = (t >> 1) & 1;
+        if (ahead.next(ha, qa, ca))
+          for (int c = 0; c < 2; ++c) tma_prefetch_l2_4d(&tm_q, c * 64, ha, qa * BM, b);
         if (t >= 2) mbar_wait(&bar.q_empty[st], ph ^ 1u, wc);
         mbar_arrive_expect_tx(&bar.q_full[st], TILE);
         for (int c = 0; c < 2; ++c)
           tma_load_4d(base + KV_OFF_Q + st * TILE + c * HALF, &tm_q, &bar.q_full[st], c * 64, h,
                       qt * BM, b);
+        ++t;
+      }
+      if (bar.abort) {
+        mbar_wait_final(&bar.kv_full, 0, a.timeout_ns);
+        for (int n = max(0, t - 2); n < t; ++n)
+          mbar_wait_final(&bar.q_full[n & 1], (n >> 1) & 1, a.timeout_ns);
+      }
+    }
+  } else if (warp == WARP_PRODUCER_2) {
+    // dO stages are freed by dV, earlier than Q stages (freed by dK): a separate warp
+    // refills them without queueing behind the Q releases
+    if (lane == 0) {
+      int h, qt, cls, t = 0;
+      ColWalk ahead = walk;   // two steps ahead: L2 prefetch of the dO tile
+      int ha, qa, ca;
+      for (int k = 0; k < 2 && ahead.next(ha, qa, ca); ++k)
+        for (int c = 0; c < 2; ++c) tma_prefetch_l2_4d(&tm_do, c * 64, ha, qa * BM, b);
+      while (walk.next(h, qt, cls)) {
+        const int st = t & 1;
+        const uint32_t ph = (t >> 1) & 1;
+        if (ahead.next(ha, qa, ca))
+          for (int c = 0; c < 2; ++c) tma_prefetch_l2_4d(&tm_do, c * 64, ha, qa * BM, b);
         if (t >= 2) mbar_wait(&bar.do_empty[st], ph ^ 1u, wc);
         mbar_arrive_expect_tx(&bar.do_full[st], TILE);
         for (int c = 0; c < 2; ++c)
@@ -276,11 +305,8 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         ++t;
       }
       if (bar.abort) {
-        mbar_wait_final(&bar.kv_full, 0, a.timeout_ns);
-        for (int n = max(0, t - 2); n < t; ++n) {
-          mbar_wait_final(&bar.q_full[n & 1], (n >> 1) & 1, a.timeout_ns);
+        for (int n = max(0, t - 2); n < t; ++n)
           mbar_wait_final(&bar.do_full[n & 1], (n >> 1) & 1, a.timeout_ns);
-        }
       }
     }
   } else if (warp == WARP_MMA) {
@@ -300,37 +326,30 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         int h, qt, cls;
         while (w2.next(h, qt, cls)) ++total;
       }
+      // Three MMA groups per (head, query tile) step t: SdP(t) = {S, dP}, dV(t), dK(t).
+      // They are issued as soon as their inputs are ready rather than in a fixed order, so
+      // a late Q/dO tile for SdP(t+1) never holds back dV(t) or dK(t).  Barrier phases
+      // cannot run ahead of the tests below: SdP(t+1) needs the softmax's release of
+      // S/dP(t); the softmax writes P(t+1) only after dK(t) completed, so p_ready and
+      // ds_ready are at most one phase beyond the step they are tested for.
       auto issue_sdp = [&](int t) {
         const int st = t & 1;
-        const uint32_t ph = (t >> 1) & 1;
         const uint64_t dq = dq_k0 + st * stage_step(TILE);
         const uint64_t ddo = ddo_k0 + st * stage_step(TILE);
-        mbar_wait(&bar.q_full[st], ph, wc);
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk)
           umma_bf16_ss(tmem + KV_TM_S, dq + kmajor_step(kk, HALF), dk_ + kmajor_step(kk, HALF),
                        IDESC_NT, kk > 0 ? 1u : 0u);
-        mbar_wait(&bar.do_full[st], ph, wc);
-        tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk)
           umma_bf16_ss(tmem + KV_TM_DP, ddo + kmajor_step(kk, HALF), dv_ + kmajor_step(kk, HALF),
                        IDESC_NT, kk > 0 ? 1u : 0u);
         umma_commit(&bar.sdp_full);
       };
-      mbar_wait(&bar.kv_full, 0, wc);
-      if (total > 0) issue_sdp(0);
-      for (int t = 0; t < total; ++t) {
+      auto issue_dv = [&](int t) {
         const int st = t & 1;
-        const uint32_t par = t & 1;
-        if (t + 1 < total) {
-          mbar_wait(&bar.sdp_free, par, wc);
-          issue_sdp(t + 1);
-        }
-        const uint64_t dq = dq_m0 + st * stage_step(TILE);
         const uint64_t ddo = ddo_m0 + st * stage_step(TILE);
-        mbar_wait(&bar.p_ready, par, wc);
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BM / 16; ++kk)
@@ -338,7 +357,10 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                        IDESC_TT, (t > 0 || kk > 0) ? 1u : 0u);
         umma_commit(&bar.dv_done);
         umma_commit(&bar.do_empty[st]);
-        mbar_wait(&bar.ds_ready, par, wc);
+      };
+      auto issue_dk = [&](int t) {
+        const int st = t & 1;
+        const uint64_t dq = dq_m0 + st * stage_step(TILE);
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BM / 16; ++kk)
@@ -346,6 +368,34 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                        IDESC_TT, (t > 0 || kk > 0) ? 1u : 0u);
         umma_commit(&bar.dk_done);
         umma_commit(&bar.q_empty[st]);
+      };
+      mbar_wait(&bar.kv_full, 0, wc);
+      int t_sdp = 0, t_dv = 0, t_dk = 0;
+      uint64_t idle_since = 0;
+      while (t_dk < total && !bar.abort) {
+        bool progress = false;
+        if (t_sdp < total && (t_sdp == 0 || mbar_test(&bar.sdp_free, (t_sdp - 1) & 1)) &&
+            mbar_test(&bar.q_full[t_sdp & 1], (t_sdp >> 1) & 1) &&
+            mbar_test(&bar.do_full[t_sdp & 1], (t_sdp >> 1) & 1)) {
+          issue_sdp(t_sdp++);
+          progress = true;
+        }
+        if (t_dv < t_sdp && mbar_test(&bar.p_ready, t_dv & 1)) {
+          issue_dv(t_dv++);
+          progress = true;
+        }
+        if (t_dk < t_dv && mbar_test(&bar.ds_ready, t_dk & 1)) {
+          issue_dk(t_dk++);
+          progress = true;
+        }
+        if (progress) {
+          idle_since = 0;
+        } else if (idle_since == 0) {
+          idle_since = globaltimer_ns();
+        } else if (globaltimer_ns() - idle_since > a.timeout_ns) {
+          bar.abort = 1;
+          atomicOr(a.err, LCA_DEVERR_TIMEOUT);
+        }
       }
     }
   } else {
@@ -355,23 +405,34 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const uint32_t spds = base_u32 + KV_OFF_PDS + half * HALF;
     const float sl2 = dm.scale_log2;
     const int c0 = kt * BN + half * 64;
+    // LSE and D of the next pair are loaded one iteration ahead so their global-memory
+    // latency overlaps the current pair's work.
     int h, qt, cls, t = 0;
-    while (walk.next(h, qt, cls)) {
+    bool have = walk.next(h, qt, cls);
+    float lse_next = 0.f, dsum_next = 0.f;
+    auto load_rows = [&](int hh, int qq) {
+      const int ii = qq * BM + row;
+      if (ii < S) {
+        const int64_t ri = (static_cast<int64_t>(b) * dm.h_q + hh) * S + ii;
+        lse_next = __ldg(a.lse + ri);
+        dsum_next = __ldg(a.dsum + ri);
+      }
+    };
+    if (have) load_rows(h, qt);
+    while (have) {
       const int i = qt * BM + row;
       const bool valid = i < S;
-      const int64_t rowi = (static_cast<int64_t>(b) * dm.h_q + h) * S + i;
-      float lse2 = INFINITY, dsum = 0.f;
-      if (valid) {
-        const float l = __ldg(a.lse + rowi);
-        lse2 = (l == -INFINITY) ? INFINITY : l * LOG2E;
-        dsum = __ldg(a.dsum + rowi);
-      }
+      const float lse2 = (!valid || lse_next == -INFINITY) ? INFINITY : lse_next * LOG2E;
+      const float dsum = valid ? dsum_next : 0.f;
       const bool masked = cls != LCA_TILE_FULL || kt * BN + BN > S || qt * BM + BM > S;
       uint32_t bits[2] = {0u, 0u};
       if (masked && valid) {
         const RowSpan sp = row_span(a.mask, i);
         row_tile_bits<2>(a.mask, h / dm.heads_per_map, i, c0, sp, bits);
       }
+      int h_n, qt_n, cls_n;
+      const bool have_n = walk.next(h_n, qt_n, cls_n);
+      if (have_n) load_rows(h_n, qt_n);
       mbar_wait(&bar.sdp_full, t & 1, wc);
       __syncwarp();
       tc_fence_after();
@@ -392,6 +453,10 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       fence_proxy_async_smem();
       mbar_arrive(&bar.ds_ready);
       ++t;
+      have = have_n;
+      h = h_n;
+      qt = qt_n;
+      cls = cls_n;
     }
     if (t > 0) {
       mbar_wait(&bar.dk_done, (t - 1) & 1, wc);
@@ -494,6 +559,10 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const int kt = __ldg(pl.kt_idx + beg + n);
         const int st = n & 1;
         const uint32_t ph = (n >> 1) & 1;
+        if (n + 2 < n_tiles) {
+          const int ka = __ldg(pl.kt_idx + beg + n + 2);
+          for (int c = 0; c < 2; ++c) tma_prefetch_l2_4d(&tm_k, c * 64, hk, ka * BN, b);
+        }
         if (n >= 2) mbar_wait(&bar.k_empty[st], ph ^ 1u, wc);
         mbar_arrive_expect_tx(&bar.k_full[st], TILE);
         for (int c = 0; c < 2; ++c)
@@ -514,6 +583,10 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const int kt = __ldg(pl.kt_idx + beg + n);
         const int st = n & 1;
         const uint32_t ph = (n >> 1) & 1;
+        if (n + 2 < n_tiles) {
+          const int ka = __ldg(pl.kt_idx + beg + n + 2);
+          for (int c = 0; c < 2; ++c) tma_prefetch_l2_4d(&tm_v, c * 64, hk, ka * BN, b);
+        }
         if (n >= 2) mbar_wait(&bar.v_empty[st], ph ^ 1u, wc);
         mbar_arrive_expect_tx(&bar.v_full[st], TILE);
         for (int c = 0; c < 2; ++c)

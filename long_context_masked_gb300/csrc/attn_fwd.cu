@@ -149,6 +149,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       for (int n = 0; n < n_tiles; ++n) {
         const int kt = __ldg(pl.kt_idx + beg + n);
         const int ks = n % KST;
+        if (n + KST < n_tiles) {   // L2 prefetch one ring ahead
+          const int ka = __ldg(pl.kt_idx + beg + n + KST);
+          for (int c = 0; c < 2; ++c) tma_prefetch_l2_4d(&tm_k, c * 64, hk, ka * BN, b);
+        }
         if (n >= KST) mbar_wait(&bar.k_empty[ks], (n / KST - 1) & 1, wc);
         mbar_arrive_expect_tx(&bar.k_full[ks], TILE_BYTES);
         for (int c = 0; c < 2; ++c)
@@ -165,6 +169,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       for (int n = 0; n < n_tiles; ++n) {
         const int kt = __ldg(pl.kt_idx + beg + n);
         const int vs = n % VST;
+        if (n + VST < n_tiles) {
+          const int ka = __ldg(pl.kt_idx + beg + n + VST);
+          for (int c = 0; c < 2; ++c) tma_prefetch_l2_4d(&tm_v, c * 64, hk, ka * BN, b);
+        }
         if (n >= VST) mbar_wait(&bar.v_empty[vs], (n / VST - 1) & 1, wc);
         mbar_arrive_expect_tx(&bar.v_full[vs], TILE_BYTES);
         for (int c = 0; c < 2; ++c)
