@@ -481,18 +481,20 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
 // ------------------------------------------------------------------ dQ
 
+constexpr int DQ_KST = 3;                        // K stages (K is held until the dQ MMA)
+constexpr int DQ_VST = 2;                        // V stages (V is released after dP)
 constexpr uint32_t DQ_OFF_Q = 0;
 constexpr uint32_t DQ_OFF_DO = TILE;
-constexpr uint32_t DQ_OFF_K = 2 * TILE;        // 2 stages
-constexpr uint32_t DQ_OFF_V = 4 * TILE;        // 2 stages
-constexpr uint32_t DQ_OFF_BAR = 6 * TILE;
-constexpr uint32_t DQ_SMEM = DQ_OFF_BAR + 256 + 1024;
+constexpr uint32_t DQ_OFF_K = 2 * TILE;
+constexpr uint32_t DQ_OFF_V = DQ_OFF_K + DQ_KST * TILE;
+constexpr uint32_t DQ_OFF_BAR = DQ_OFF_V + DQ_VST * TILE;
+constexpr uint32_t DQ_SMEM = DQ_OFF_BAR + 256;    // the dynamic base is 1024-aligned
 static_assert(DQ_SMEM <= 232448, "dynamic shared memory above the 227 KB per-CTA limit");
 constexpr uint32_t DQ_TM_S = 0, DQ_TM_DP = 128, DQ_TM_DQ = 256, DQ_TM_DS = 384;
 
 struct DqBars {
   uint64_t qdo_full;
-  uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
+  uint64_t k_full[DQ_KST], k_empty[DQ_KST], v_full[DQ_VST], v_empty[DQ_VST];
   uint64_t sdp_full, sdp_free, ds_ready, dq_done;
   uint32_t tmem_base;
   int abort;
@@ -502,9 +504,13 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
 bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
               BwdArgs a) {
-  extern __shared__ uint8_t smem_raw[];
-  uint32_t base_u32;
-  uint8_t* base = aligned_smem(smem_raw, base_u32);
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t base_u32 = smem_u32(smem_raw);
+  if (base_u32 & 1023u) {   // the swizzled tiles need a 1024-byte-aligned base
+    if (threadIdx.x == 0) atomicOr(a.err, LCA_DEVERR_LAYOUT);
+    return;
+  }
+  uint8_t* base = smem_raw;
   DqBars& bar = *reinterpret_cast<DqBars*>(base + DQ_OFF_BAR);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const AttnDims& dm = a.dims;
@@ -525,9 +531,11 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 
   if (threadIdx.x == 0) {
     mbar_init(&bar.qdo_full, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < DQ_KST; ++s) {
       mbar_init(&bar.k_full[s], 1);
       mbar_init(&bar.k_empty[s], 1);
+    }
+    for (int s = 0; s < DQ_VST; ++s) {
       mbar_init(&bar.v_full[s], 1);
       mbar_init(&bar.v_empty[s], 1);
     }
@@ -557,13 +565,12 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       }
       for (int n = 0; n < n_tiles; ++n) {
         const int kt = __ldg(pl.kt_idx + beg + n);
-        const int st = n & 1;
-        const uint32_t ph = (n >> 1) & 1;
-        if (n + 2 < n_tiles) {
-          const int ka = __ldg(pl.kt_idx + beg + n + 2);
+        const int st = n % DQ_KST;
+        if (n + DQ_KST < n_tiles) {
+          const int ka = __ldg(pl.kt_idx + beg + n + DQ_KST);
           for (int c = 0; c < 2; ++c) tma_prefetch_l2_4d(&tm_k, c * 64, hk, ka * BN, b);
         }
-        if (n >= 2) mbar_wait(&bar.k_empty[st], ph ^ 1u, wc);
+        if (n >= DQ_KST) mbar_wait(&bar.k_empty[st], (n / DQ_KST - 1) & 1, wc);
         mbar_arrive_expect_tx(&bar.k_full[st], TILE);
         for (int c = 0; c < 2; ++c)
           tma_load_4d(base + DQ_OFF_K + st * TILE + c * HALF, &tm_k, &bar.k_full[st], c * 64, hk,
@@ -571,8 +578,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       }
       if (bar.abort) {
         mbar_wait_final(&bar.qdo_full, 0, a.timeout_ns);
-        for (int n = max(0, n_tiles - 2); n < n_tiles; ++n)
-          mbar_wait_final(&bar.k_full[n & 1], (n >> 1) & 1, a.timeout_ns);
+        for (int n = max(0, n_tiles - DQ_KST); n < n_tiles; ++n)
+          mbar_wait_final(&bar.k_full[n % DQ_KST], (n / DQ_KST) & 1, a.timeout_ns);
       }
     }
   } else if (warp == WARP_PRODUCER_2) {
@@ -581,21 +588,20 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       // a separate warp keeps V loads from queueing behind K releases
       for (int n = 0; n < n_tiles; ++n) {
         const int kt = __ldg(pl.kt_idx + beg + n);
-        const int st = n & 1;
-        const uint32_t ph = (n >> 1) & 1;
-        if (n + 2 < n_tiles) {
-          const int ka = __ldg(pl.kt_idx + beg + n + 2);
+        const int st = n % DQ_VST;
+        if (n + DQ_VST < n_tiles) {
+          const int ka = __ldg(pl.kt_idx + beg + n + DQ_VST);
           for (int c = 0; c < 2; ++c) tma_prefetch_l2_4d(&tm_v, c * 64, hk, ka * BN, b);
         }
-        if (n >= 2) mbar_wait(&bar.v_empty[st], ph ^ 1u, wc);
+        if (n >= DQ_VST) mbar_wait(&bar.v_empty[st], (n / DQ_VST - 1) & 1, wc);
         mbar_arrive_expect_tx(&bar.v_full[st], TILE);
         for (int c = 0; c < 2; ++c)
           tma_load_4d(base + DQ_OFF_V + st * TILE + c * HALF, &tm_v, &bar.v_full[st], c * 64, hk,
                       kt * BN, b);
       }
       if (bar.abort) {
-        for (int n = max(0, n_tiles - 2); n < n_tiles; ++n)
-          mbar_wait_final(&bar.v_full[n & 1], (n >> 1) & 1, a.timeout_ns);
+        for (int n = max(0, n_tiles - DQ_VST); n < n_tiles; ++n)
+          mbar_wait_final(&bar.v_full[n % DQ_VST], (n / DQ_VST) & 1, a.timeout_ns);
       }
     }
   } else if (warp == WARP_MMA) {
@@ -607,44 +613,58 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       const uint64_t dk_k0 = desc_kmajor(base_u32 + DQ_OFF_K, 0, HALF);
       const uint64_t dk_m0 = desc_mnmajor(base_u32 + DQ_OFF_K, 0, HALF);
       const uint64_t dv_k0 = desc_kmajor(base_u32 + DQ_OFF_V, 0, HALF);
+      // Two MMA groups per key tile n: SdP(n) = {S, dP} and dQ(n), issued as soon as
+      // their inputs are ready so that a late K/V tile for SdP(n+1) never holds back
+      // dQ(n).  SdP(n+1) needs the softmax's release of S/dP(n); the softmax writes
+      // dS(n+1) only after dQ(n) completed, so ds_ready is at most one phase ahead.
       auto issue_sdp = [&](int n) {
-        const int st = n & 1;
-        const uint32_t ph = (n >> 1) & 1;
-        const uint64_t dk = dk_k0 + st * stage_step(TILE);
-        const uint64_t dv = dv_k0 + st * stage_step(TILE);
-        mbar_wait(&bar.k_full[st], ph, wc);
+        const uint64_t dk = dk_k0 + (n % DQ_KST) * stage_step(TILE);
+        const uint64_t dv = dv_k0 + (n % DQ_VST) * stage_step(TILE);
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk)
           umma_bf16_ss(tmem + DQ_TM_S, dq_ + kmajor_step(kk, HALF), dk + kmajor_step(kk, HALF),
                        IDESC_NT, kk > 0 ? 1u : 0u);
-        mbar_wait(&bar.v_full[st], ph, wc);
-        tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk)
           umma_bf16_ss(tmem + DQ_TM_DP, ddo_ + kmajor_step(kk, HALF), dv + kmajor_step(kk, HALF),
                        IDESC_NT, kk > 0 ? 1u : 0u);
         umma_commit(&bar.sdp_full);
-        umma_commit(&bar.v_empty[st]);
+        umma_commit(&bar.v_empty[n % DQ_VST]);
       };
-      mbar_wait(&bar.qdo_full, 0, wc);
-      if (n_tiles > 0) issue_sdp(0);
-      for (int n = 0; n < n_tiles; ++n) {
-        const int st = n & 1;
-        const uint32_t par = n & 1;
-        if (n + 1 < n_tiles) {
-          mbar_wait(&bar.sdp_free, par, wc);
-          issue_sdp(n + 1);
-        }
-        const uint64_t dk = dk_m0 + st * stage_step(TILE);
-        mbar_wait(&bar.ds_ready, par, wc);
+      auto issue_dq = [&](int n) {
+        const uint64_t dk = dk_m0 + (n % DQ_KST) * stage_step(TILE);
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
           umma_bf16_ts(tmem + DQ_TM_DQ, tmem + DQ_TM_DS + kk * 8, dk + mnmajor_step(kk),
                        IDESC_NN, (n > 0 || kk > 0) ? 1u : 0u);
         umma_commit(&bar.dq_done);
-        umma_commit(&bar.k_empty[st]);
+        umma_commit(&bar.k_empty[n % DQ_KST]);
+      };
+      mbar_wait(&bar.qdo_full, 0, wc);
+      int n_sdp = 0, n_dq = 0;
+      uint64_t idle_since = 0;
+      while (n_dq < n_tiles && !bar.abort) {
+        bool progress = false;
+        if (n_sdp < n_tiles && (n_sdp == 0 || mbar_test(&bar.sdp_free, (n_sdp - 1) & 1)) &&
+            mbar_test(&bar.k_full[n_sdp % DQ_KST], (n_sdp / DQ_KST) & 1) &&
+            mbar_test(&bar.v_full[n_sdp % DQ_VST], (n_sdp / DQ_VST) & 1)) {
+          issue_sdp(n_sdp++);
+          progress = true;
+        }
+        if (n_dq < n_sdp && mbar_test(&bar.ds_ready, n_dq & 1)) {
+          issue_dq(n_dq++);
+          progress = true;
+        }
+        if (progress) {
+          idle_since = 0;
+        } else if (idle_since == 0) {
+          idle_since = globaltimer_ns();
+        } else if (globaltimer_ns() - idle_since > a.timeout_ns) {
+          bar.abort = 1;
+          atomicOr(a.err, LCA_DEVERR_TIMEOUT);
+        }
       }
     }
   } else {
