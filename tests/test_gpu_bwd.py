@@ -150,3 +150,24 @@ def test_heterogeneous_full_size(mask, kw):
     plan, _, grads = _run(desc, dev)
     _sampled_dq(desc, host, grads, heads=[0, 40], nrows=16, seed=mask)
     _invariants(desc, host, dev, grads, plan)
+
+
+@pytest.mark.parametrize("s,block,hq,hkv,sparsity", [(131072, 64, 64, 8, 0.5), (65536, 128, 32, 32, 0.8),
+                                                     (32768, 64, 32, 32, 0.2)])
+def test_uniform_block_sparse_full_size(s, block, hq, hkv, sparsity):
+    map_heads = hkv if hq != hkv else hq
+    host, dev = make_inputs(1, s, hq, hkv, seed=500 + block)
+    desc = I.make_desc(I.BLOCK_SPARSE_UNIFORM, s, sparse_block=block, sparsity=sparsity,
+                       map_heads=map_heads, map_seed=block)
+    plan, _, grads = _run(desc, dev)
+    _sampled_dq(desc, host, grads, heads=[0, hq - 1], nrows=12, seed=block)
+    _invariants(desc, host, dev, grads, plan)
+
+
+def test_variable_block_sparse_long_varlen():
+    s = 131072
+    host, dev = make_inputs(1, s, 64, 8, seed=600)
+    desc = I.make_desc(I.BLOCK_SPARSE_VARIABLE, s, map_heads=8, map_seed=7, doc_seed=7)
+    plan, _, grads = _run(desc, dev)
+    _sampled_dq(desc, host, grads, heads=[0, 37], nrows=12, seed=7)
+    _invariants(desc, host, dev, grads, plan)

@@ -119,3 +119,18 @@ def test_heterogeneous_full_size_sampled(mask, kw):
     s = 32768
     desc = I.make_desc(mask, s, **kw)
     _sampled(desc, 1, s, 64, 64, heads=[0, 31, 63], nrows=40, seed=200 + mask)
+
+
+@pytest.mark.parametrize("s,block,hq,hkv,sparsity", [(131072, 64, 64, 8, 0.5), (65536, 128, 32, 32, 0.8),
+                                                     (32768, 64, 32, 32, 0.2)])
+def test_uniform_block_sparse_full_size_sampled(s, block, hq, hkv, sparsity):
+    map_heads = hkv if hq != hkv else hq
+    desc = I.make_desc(I.BLOCK_SPARSE_UNIFORM, s, sparse_block=block, sparsity=sparsity,
+                       map_heads=map_heads, map_seed=block)
+    _sampled(desc, 1, s, hq, hkv, heads=[0, hq - 1], nrows=24, seed=s + block)
+
+
+def test_variable_block_sparse_long_varlen_sampled():
+    s = 131072
+    desc = I.make_desc(I.BLOCK_SPARSE_VARIABLE, s, map_heads=8, map_seed=7, doc_seed=7)
+    _sampled(desc, 1, s, 64, 8, heads=[0, 37], nrows=24, seed=99)
