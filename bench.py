@@ -3,7 +3,7 @@
 
 Metric: TFLOP/s on unmasked FLOPs - 4*d*H_q per allowed (i, j) pair forward and
 2.5x that backward - per mask and sequence length, plus the fraction of the GB300
-bf16 dense tensor peak.  The workload is the benchmark's dense regular masks
+bf16 dense tensor peak.  The default workload is the benchmark's dense regular masks
 (LongCA-bench, sections 2.1 and A.4: FULL, CAUSAL, sliding window, full/causal
 document over lognormal-length documents) on GQA 64:8, d = 128, at S = 8K, 16K, 32K
 and 48K.  One step runs, for every (S, mask): the tile plan build, the forward and the
@@ -11,9 +11,15 @@ backward, on synthetic N(0, 1) bf16 inputs resident on the GPU.  Document masks
 re-draw their lengths every step (seed = step mod 30; the pages sample 30 runs).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--suite dense|heterogeneous|sparse|varlen] [--case S:MASK]
 
-``--impl reference`` times the fp64 CPU oracle (the only reference available here)
-on a bounded row sample of the same workload.  Prints one JSON line (rank 0).
+``--suite`` selects another of the benchmark's workloads: the heterogeneous static
+masks at S = 32K on MHA 64:64; uniform block-sparse maps (blocks 64/128, sparsity
+0.2/0.5/0.8, S = 32K-128K, GQA 64:8 and MHA 32:32), reported per case with the
+fraction of non-skipped tiles and the time per tile; or S = 128K documents with
+variable block-sparse maps.  ``--impl reference`` times the fp64 CPU oracle (the only
+reference available here) on a bounded row sample of the selected workload.  Prints
+one JSON line (rank 0).
 """
 from __future__ import annotations
 
@@ -25,7 +31,6 @@ os.environ.setdefault("OMP_NUM_THREADS", str(os.cpu_count() or 1))
 import argparse  # noqa: E402
 import hashlib  # noqa: E402
 import json  # noqa: E402
-import math  # noqa: E402
 import re  # noqa: E402
 import statistics  # noqa: E402
 import subprocess  # noqa: E402
@@ -41,23 +46,96 @@ from long_context_masked_gb300 import inputs as I  # noqa: E402
 
 METRIC = "attn fwd/bwd TFLOPs/s on unmasked FLOPs per mask & seqlen; % of bf16 peak"
 UNIT = "TFLOP/s"
-HQ, HKV, D = 64, 8, 128
-SEQLENS = (8192, 16384, 32768, 49152)
-MASKS = (("FULL", I.FULL, {}), ("CAUSAL", I.CAUSAL, {}),
-         ("SLIDING_WINDOW", I.SLIDING_WINDOW, {"window": 4096}),
-         ("FULL_DOCUMENT", I.FULL_DOCUMENT, {}), ("CAUSAL_DOCUMENT", I.CAUSAL_DOCUMENT, {}))
+D = 128
 DOC_RUNS = 30
-WORKLOAD = ("dense regular masks (FULL, CAUSAL, SLIDING_WINDOW w=4096, FULL_DOCUMENT, "
-            "CAUSAL_DOCUMENT with lognormal(ln 2048, 1) documents clipped to [128, S]), "
-            "GQA 64:8, d=128, B=1 per GPU, S in {8K, 16K, 32K, 48K}")
 FLUSH_BYTES = 256 << 20
+FWD_PER_PAIR, BWD_PER_PAIR = 4.0 * D, 10.0 * D
 KERNEL_SOURCES = {"attn_fwd": "attn_fwd.cu", "bwd_dkdv": "attn_bwd.cu", "bwd_dq": "attn_bwd.cu",
                   "bwd_preprocess": "attn_bwd.cu"}
+SUITES = ("dense", "heterogeneous", "sparse", "varlen")
 
 
-def desc_for(mask_type, s, kw, step):
-    seed = step % DOC_RUNS
-    return I.make_desc(mask_type, s, doc_seed=seed, **kw)
+# ------------------------------------------------------------------ workloads
+#
+# A workload is a list of groups (S, H_q, H_kv, cases).  Every group shares one set of
+# resident tensors; a case is (name, make, per_step) where make(seed) returns the mask
+# descriptor and per_step says whether the descriptor is re-drawn every step.
+
+class Case:
+    def __init__(self, name, make, per_step=False):
+        self.name, self.make, self.per_step = name, make, per_step
+
+
+def dense_cases(s):
+    return [Case("FULL", lambda st: I.make_desc(I.FULL, s)),
+            Case("CAUSAL", lambda st: I.make_desc(I.CAUSAL, s)),
+            Case("SLIDING_WINDOW", lambda st: I.make_desc(I.SLIDING_WINDOW, s, window=4096)),
+            Case("FULL_DOCUMENT", lambda st: I.make_desc(I.FULL_DOCUMENT, s, doc_seed=st), True),
+            Case("CAUSAL_DOCUMENT", lambda st: I.make_desc(I.CAUSAL_DOCUMENT, s, doc_seed=st),
+                 True)]
+
+
+def heterogeneous_cases(s):
+    return [Case("PREFIX_LM", lambda st: I.make_desc(I.PREFIX_LM, s, prefix_len=s // 4)),
+            Case("SHARED_QUESTION",
+                 lambda st: I.make_desc(I.SHARED_QUESTION, s, question=2048,
+                                        answers=[(s - 2048) // 4] * 4)),
+            Case("GLOBAL_SLIDING",
+                 lambda st: I.make_desc(I.GLOBAL_SLIDING, s, num_global=256, window=4096)),
+            Case("CAUSAL_BLOCKWISE", lambda st: I.make_desc(I.CAUSAL_BLOCKWISE, s, block=2048)),
+            Case("BLOCK_CAUSAL_DOCUMENT",
+                 lambda st: I.make_desc(I.BLOCK_CAUSAL_DOCUMENT, s, block=2048, doc_seed=st),
+                 True)]
+
+
+def sparse_cases(s, map_heads):
+    out = []
+    for b in (64, 128):
+        for sp in (0.2, 0.5, 0.8):
+            out.append(Case(f"UNIFORM_b{b}_s{sp}",
+                            lambda st, b=b, sp=sp: I.make_desc(
+                                I.BLOCK_SPARSE_UNIFORM, s, sparse_block=b, sparsity=sp,
+                                map_heads=map_heads, map_seed=1000 * b + int(10 * sp))))
+    return out
+
+
+def workload(suite, case=None):
+    """(groups, description) of a named workload, or of one S:MASK dense case."""
+    if case is not None:
+        s_txt, m_txt = case.split(":")
+        s = int(s_txt)
+        cases = [c for c in dense_cases(s) if c.name == m_txt]
+        if not cases:
+            raise SystemExit(f"unknown mask {m_txt}")
+        return [(s, 64, 8, cases)], f"single case {case} (GQA 64:8, d=128)"
+    if suite == "dense":
+        return ([(s, 64, 8, dense_cases(s)) for s in (8192, 16384, 32768, 49152)],
+                "dense regular masks (FULL, CAUSAL, SLIDING_WINDOW w=4096, FULL_DOCUMENT, "
+                "CAUSAL_DOCUMENT with lognormal(ln 2048, 1) documents clipped to [128, S]), "
+                "GQA 64:8, d=128, B=1 per GPU, S in {8K, 16K, 32K, 48K}")
+    if suite == "heterogeneous":
+        return ([(32768, 64, 64, heterogeneous_cases(32768))],
+                "heterogeneous static masks, S=32K, MHA 64:64, d=128: PREFIX_LM (prefix 8K), "
+                "SHARED_QUESTION (2K question + 4 x 7.5K answers), GLOBAL_SLIDING (256 global, "
+                "w=4096), CAUSAL_BLOCKWISE (2K blocks), BLOCK_CAUSAL_DOCUMENT (2K blocks in "
+                "lognormal documents)")
+    if suite == "sparse":
+        groups = []
+        for s in (32768, 65536, 131072):
+            groups.append((s, 64, 8, sparse_cases(s, 8)))
+            groups.append((s, 32, 32, sparse_cases(s, 32)))
+        return (groups, "uniform block-sparse maps (Bernoulli keep, diagonal blocks kept), "
+                        "blocks 64/128, sparsity 0.2/0.5/0.8, S in {32K, 64K, 128K}, GQA 64:8 "
+                        "(one map per KV head) and MHA 32:32 (one map per head), d=128")
+    if suite == "varlen":
+        return ([(131072, 64, 8, [Case("CAUSAL_DOCUMENT+VARIABLE_BLOCKS",
+                                       lambda st: I.make_desc(I.BLOCK_SPARSE_VARIABLE, 131072,
+                                                              map_heads=8, map_seed=st,
+                                                              doc_seed=st), True)])],
+                "S=128K, GQA 64:8, d=128: CAUSAL_DOCUMENT (lognormal documents) AND one "
+                "variable block partition per KV head (block sizes 32..256, multiples of 16) "
+                "with 50% of the causal blocks kept")
+    raise ValueError(suite)
 
 
 def peaks():
@@ -83,6 +161,7 @@ class ClockSampler:
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
+        self.out = ""
 
     def __enter__(self):
         try:
@@ -95,7 +174,6 @@ class ClockSampler:
         return self
 
     def __exit__(self, *exc):
-        self.out = ""
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -130,50 +208,64 @@ class ClockSampler:
 _ORACLE_INPUTS = {}
 
 
-def oracle_sample(rows_per_combo, seed=0, budget_s=None):
+def first_map_head(desc):
+    """The descriptor restricted to its first map head (query head 0 uses it)."""
+    if desc.map_heads == 1:
+        return desc
+    cut = {"map_heads": 1, "block_map": desc.block_map[:1]}
+    for name in ("row_offsets", "col_offsets"):
+        if getattr(desc, name) is not None:
+            cut[name] = getattr(desc, name)[:1]
+    return I.MaskDesc(**{**desc.__dict__, **cut})
+
+
+def oracle_sample(groups, rows_per_case, seed=0, budget_s=None):
     """Time the fp64 oracle on a bounded sample of the workload.
 
-    Sample: for every (S, mask) of the workload, query head 0 and ``rows_per_combo``
-    whole query rows from the middle of the sequence (all keys), forward and
-    backward.  Credited FLOPs: 14*d per allowed pair of the sampled rows.
+    Sample: for every case of the workload, query head 0 (with its KV head and map)
+    and ``rows_per_case`` whole query rows from the middle of the sequence (all keys),
+    forward and backward.  Credited FLOPs: 14*d per allowed pair of the sampled rows.
+    Stops starting new cases once ``budget_s`` seconds are spent.
     Returns (TFLOP/s, seconds, description).
     """
     import oracle
 
     flops = 0.0
     secs = 0.0
-    done = 0
-    for s in SEQLENS:
-        if s not in _ORACLE_INPUTS:
-            _ORACLE_INPUTS[s] = tuple(x.float().numpy() for x in I.qkv_do(1, s, 8, 1, D, s))
-        q, k, v, do = _ORACLE_INPUTS[s]
-        for _, t, kw in MASKS:
-            desc = desc_for(t, s, kw, seed)
+    done = total = 0
+    for s, hq, hkv, cases in groups:
+        key = (s, hq // hkv)
+        if key not in _ORACLE_INPUTS:
+            _ORACLE_INPUTS[key] = tuple(x.float().numpy()
+                                        for x in I.qkv_do(1, s, hq // hkv, 1, D, s))
+        q, k, v, do = _ORACLE_INPUTS[key]
+        for c in cases:
+            total += 1
+            if budget_s is not None and secs > budget_s:
+                continue
+            desc = first_map_head(c.make(seed % DOC_RUNS))
             r0 = s // 2
-            r1 = min(s, r0 + rows_per_combo)
+            r1 = min(s, r0 + rows_per_case)
             t0 = time.perf_counter()
             oracle.attn_bwd_ref(q, k, v, do, desc, heads=[0], row_range=(r0, r1))
             secs += time.perf_counter() - t0
             n_pairs = int(np.count_nonzero(oracle.mask_rows(desc, 0, np.arange(r0, r1))))
             flops += 14.0 * D * n_pairs
             done += 1
-            if budget_s is not None and secs > budget_s:
-                break
-        if budget_s is not None and secs > budget_s:
-            break
-    what = (f"fp64 NumPy oracle fwd+bwd, query head 0, {rows_per_combo} middle rows x all keys, "
-            f"{done} of {len(SEQLENS) * len(MASKS)} (S, mask) combos")
+    what = (f"fp64 NumPy oracle fwd+bwd, query head 0, {rows_per_case} middle rows x all keys, "
+            f"{done} of {total} cases")
     return flops / secs / 1e12, secs, what
 
 
 def run_reference(args, rank):
     if rank != 0:
         return
+    groups, text = workload(args.suite, args.case)
     for _ in range(args.warmup):
-        oracle_sample(64, seed=0)
+        oracle_sample(groups, 64, seed=0)
     vals, secs = [], []
     for step in range(args.steps):
-        v, s, what = oracle_sample(64, seed=step)
+        v, s, what = oracle_sample(groups, 64, seed=step)
         vals.append(v)
         secs.append(s)
     value = statistics.median(vals)
@@ -182,7 +274,7 @@ def run_reference(args, rank):
             "ms_per_step": 1e3 * statistics.median(secs), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded N(0,1) bf16 inputs; lognormal documents)",
-            "config": {"workload": WORKLOAD, "l2": "n/a (CPU)"},
+            "config": {"workload": text, "suite": args.suite, "l2": "n/a (CPU)"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(),
                              "kind": "oracle", "sample": what},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -192,9 +284,9 @@ def run_reference(args, rank):
 
 # ------------------------------------------------------------------ GPU arm
 
-def traffic_from_profiles(kernel):
-    """DRAM bytes per launch of `kernel` recorded under profiles/, if the recording
-    matches the kernel's current source (sha256 prefix), else None."""
+def traffic_from_profiles(kernel, tag):
+    """DRAM bytes per launch of `kernel` recorded under profiles/ for workload `tag`, if
+    the recording matches the kernel's current source (sha256 prefix), else None."""
     src = os.path.join(ROOT, "long_context_masked_gb300", "csrc", KERNEL_SOURCES.get(kernel, ""))
     try:
         with open(src, "rb") as f:
@@ -211,9 +303,32 @@ def traffic_from_profiles(kernel):
             continue
         with open(os.path.join(pdir, name)) as f:
             for m in pat.finditer(f.read()):
-                if m.group(1) == kernel and m.group(3) == sha and m.group(4) == "bench_default":
+                if m.group(1) == kernel and m.group(3) == sha and m.group(4) == tag:
                     return int(m.group(2))
     return None
+
+
+def aggregate(flops, ms, dist=None, device=None):
+    """Whole-job totals under weak scaling: FLOPs summed over ranks, time the maximum
+    over ranks (every rank runs its own batch entry; there is no data-path collective,
+    only this reduction of the measurements)."""
+    if dist is None or not dist.is_initialized():
+        return float(flops), float(ms)
+    import torch
+
+    t = torch.tensor([float(flops)], dtype=torch.float64, device=device)
+    m = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    dist.all_reduce(m, op=dist.ReduceOp.MAX)
+    return float(t.item()), float(m.item())
+
+
+def tflops(flops, ms):
+    return flops / (ms * 1e-3) / 1e12
+
+
+def case_label(suite, s, hq, hkv, name):
+    return f"S={s}/{name}" if suite == "dense" else f"S={s}/{hq}:{hkv}/{name}"
 
 
 def run_gpu(args, rank, world):
@@ -232,48 +347,64 @@ def run_gpu(args, rank, world):
         dist = dist_mod
         dist.init_process_group("nccl", device_id=dev)
 
+    groups, text = workload(args.suite, args.case)
+    default = args.suite == "dense" and not args.case
+    tag = "bench_default" if default else (f"case_{args.case}" if args.case else args.suite)
+
     # resident inputs (one batch entry per GPU, seeded by rank) and output buffers
-    data = {}
-    for s in SEQLENS:
-        q, k, v, do = I.qkv_do(1, s, HQ, HKV, D, seed=1000 * rank + s)
-        data[s] = {"host": (q, k, v, do),
-                   "dev": tuple(x.to(dev) for x in (q, k, v, do)),
-                   "o": torch.empty((1, s, HQ, D), dtype=torch.bfloat16, device=dev),
-                   "lse": torch.empty((1, HQ, s), dtype=torch.float32, device=dev),
-                   "dq": torch.empty((1, s, HQ, D), dtype=torch.bfloat16, device=dev),
-                   "dk": torch.empty((1, s, HKV, D), dtype=torch.bfloat16, device=dev),
-                   "dv": torch.empty((1, s, HKV, D), dtype=torch.bfloat16, device=dev),
-                   "ws": torch.empty((HQ * s,), dtype=torch.float32, device=dev)}
+    data = []
+    for s, hq, hkv, _ in groups:
+        q, k, v, do = I.qkv_do(1, s, hq, hkv, D, seed=1000 * rank + s + (hq != 64) * hq)
+        data.append({"host": (q, k, v, do) if default else None,
+                     "dev": tuple(x.to(dev) for x in (q, k, v, do)),
+                     "o": torch.empty((1, s, hq, D), dtype=torch.bfloat16, device=dev),
+                     "lse": torch.empty((1, hq, s), dtype=torch.float32, device=dev),
+                     "dq": torch.empty((1, s, hq, D), dtype=torch.bfloat16, device=dev),
+                     "dk": torch.empty((1, s, hkv, D), dtype=torch.bfloat16, device=dev),
+                     "dv": torch.empty((1, s, hkv, D), dtype=torch.bfloat16, device=dev),
+                     "ws": torch.empty((hq * s,), dtype=torch.float32, device=dev)})
+        del q, k, v, do
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
-    descs = {(s, name, st): desc_for(t, s, kw, st)
-             for s in SEQLENS for name, t, kw in MASKS for st in range(DOC_RUNS)}
+
+    # descriptors are drawn on the host before any timing
+    descs = {}
+    n_draws = min(DOC_RUNS, args.warmup + args.steps)
+    for gi, (_, _, _, cases) in enumerate(groups):
+        for ci, c in enumerate(cases):
+            for st in (range(n_draws) if c.per_step else (0,)):
+                descs[(gi, ci, st)] = c.make(st)
+
+    def desc_of(gi, ci, st):
+        return descs[(gi, ci, st % DOC_RUNS if groups[gi][3][ci].per_step else 0)]
 
     def step(st, timers=None, e2e=None):
         plans = []
-        for s in SEQLENS:
-            d = data[s]
+        for gi, (s, hq, hkv, cases) in enumerate(groups):
+            d = data[gi]
             if e2e is not None:
-                for src, dst in zip(e2e["h2d"][s], d["dev"]):
+                for src, dst in zip(e2e["h2d"][gi], d["dev"]):
                     dst.copy_(src, non_blocking=True)
             q, k, v, do = d["dev"]
-            for name, _, _ in MASKS:
+            for ci, c in enumerate(cases):
                 ev = None
                 if timers is not None:
-                    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+                    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
                     ev[0].record(stream)
-                plan = lca.mask_build(descs[(s, name, st % DOC_RUNS)], 128, 128)
-                lca.attn_fwd(plan, q, k, v, out=d["o"], lse=d["lse"])
+                plan = lca.mask_build(desc_of(gi, ci, st), 128, 128)
                 if ev is not None:
                     ev[1].record(stream)
+                lca.attn_fwd(plan, q, k, v, out=d["o"], lse=d["lse"])
+                if ev is not None:
+                    ev[2].record(stream)
                 lca.attn_bwd(plan, q, k, v, d["o"], do, d["lse"], dq=d["dq"], dk=d["dk"],
                              dv=d["dv"], workspace=d["ws"])
                 if ev is not None:
-                    ev[2].record(stream)
-                    timers.append((s, name, ev))
-                plans.append((s, name, plan))
+                    ev[3].record(stream)
+                    timers.append((gi, c.name, ev))
+                plans.append((gi, c.name, plan))
             if e2e is not None:
-                for src, dst in zip((d["o"], d["lse"], d["dq"], d["dk"], d["dv"]), e2e["d2h"][s]):
+                for src, dst in zip((d["o"], d["lse"], d["dq"], d["dk"], d["dv"]), e2e["d2h"][gi]):
                     dst.copy_(src, non_blocking=True)
         return plans
 
@@ -283,111 +414,127 @@ def run_gpu(args, rank, world):
             dist.barrier()
         torch.cuda.synchronize()
 
-    def max_over_ranks(x):
-        if dist is None:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+    def pair_counts(plans):
+        """(gi, name, query-head pairs, plan info) per plan; drops the plans."""
+        return [(gi, name, int(p.n_valid().sum()) * (groups[gi][1] // p.info["map_heads"]),
+                 dict(p.info)) for gi, name, p in plans]
 
     for w in range(args.warmup):
         step(w)
     sync_all()
 
     # ---- device-resident timed steps
+    torch.cuda.reset_peak_memory_stats(dev)
     lca.profile_enable(True)
     lca.profile_read()
-    step_ms, timers, plans = [], [], []
+    step_ms, counts, timers = [], [], []
     with ClockSampler(local) as clk:
         for st in range(args.steps):
             flush.zero_()
             sync_all()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            plans.append(step(st, timers))
+            plans = step(st, timers)
             e1.record(stream)
             sync_all()
             step_ms.append(e0.elapsed_time(e1))
+            counts.append(pair_counts(plans))
+            del plans
     prof = lca.profile_read()
     lca.profile_enable(False)
     clocks = clk.summary()
+    peak_mem = torch.cuda.max_memory_allocated(dev)
 
     # credited FLOPs from the plans' exact pair counts
-    pairs = {}
-    total_pairs = 0
-    for st_plans in plans:
-        for s, name, plan in st_plans:
-            nv = plan.export()["n_valid"]
-            hsum = int(nv.sum()) * (HQ // plan.info["map_heads"])
-            pairs.setdefault((s, name), []).append(hsum)
-            total_pairs += hsum
-    fwd_per_pair, bwd_per_pair = 4.0 * D, 10.0 * D
-    total_flops = total_pairs * (fwd_per_pair + bwd_per_pair)
-    total_ms = max_over_ranks(sum(step_ms))
-    value = world * total_flops / (total_ms * 1e-3) / 1e12
+    total_pairs = sum(c[2] for st_counts in counts for c in st_counts)
+    job_flops, total_ms = aggregate(total_pairs * (FWD_PER_PAIR + BWD_PER_PAIR), sum(step_ms),
+                                    dist, dev)
+    value = tflops(job_flops, total_ms)
     pk = peaks()
 
     per_cfg = {}
-    for idx, (s, name, ev) in enumerate(timers):
-        st = idx // (len(SEQLENS) * len(MASKS))
-        hp = pairs[(s, name)][st]
-        f_ms, b_ms = ev[0].elapsed_time(ev[1]), ev[1].elapsed_time(ev[2])
-        acc = per_cfg.setdefault(f"S={s}/{name}", {"fwd": [], "bwd": []})
-        acc["fwd"].append(fwd_per_pair * hp / (f_ms * 1e-3) / 1e12)
-        acc["bwd"].append(bwd_per_pair * hp / (b_ms * 1e-3) / 1e12)
-    per_config = {k: {"fwd_tflops": round(statistics.median(v["fwd"]), 1),
-                      "bwd_tflops": round(statistics.median(v["bwd"]), 1),
-                      "fwd_pct_peak": round(100 * statistics.median(v["fwd"]) / pk["bf16"], 1),
-                      "bwd_pct_peak": round(100 * statistics.median(v["bwd"]) / pk["bf16"], 1)}
-                  for k, v in per_cfg.items()}
+    flat = [c for st_counts in counts for c in st_counts]
+    for (gi, name, ev), (gi2, name2, hp, info) in zip(timers, flat):
+        assert (gi, name) == (gi2, name2)
+        s, hq, hkv, _ = groups[gi]
+        b_ms = ev[0].elapsed_time(ev[1])
+        f_ms = ev[1].elapsed_time(ev[2])
+        w_ms = ev[2].elapsed_time(ev[3])
+        acc = per_cfg.setdefault(case_label(args.suite, s, hq, hkv, name),
+                                 {"fwd": [], "bwd": [], "build_ms": [], "fwd_ms": [],
+                                  "bwd_ms": [], "info": info, "hq": hq})
+        acc["fwd"].append(tflops(FWD_PER_PAIR * hp, f_ms))
+        acc["bwd"].append(tflops(BWD_PER_PAIR * hp, w_ms))
+        acc["build_ms"].append(b_ms)
+        acc["fwd_ms"].append(f_ms)
+        acc["bwd_ms"].append(w_ms)
+    per_config = {}
+    for label, v in per_cfg.items():
+        fwd, bwd = statistics.median(v["fwd"]), statistics.median(v["bwd"])
+        row = {"fwd_tflops": round(fwd, 1), "bwd_tflops": round(bwd, 1),
+               "fwd_pct_peak": round(100 * fwd / pk["bf16"], 1),
+               "bwd_pct_peak": round(100 * bwd / pk["bf16"], 1),
+               "build_ms": round(statistics.median(v["build_ms"]), 3)}
+        if not default:
+            inf = v["info"]
+            head_tiles = inf["nnz"] * (v["hq"] // inf["map_heads"])
+            f_ms, w_ms = statistics.median(v["fwd_ms"]), statistics.median(v["bwd_ms"])
+            row.update({"fwd_ms": round(f_ms, 3), "bwd_ms": round(w_ms, 3),
+                        "nonskipped_tile_fraction":
+                            round(inf["nnz"] / (inf["map_heads"] * inf["n_qt"] * inf["n_kt"]), 4),
+                        "fwd_us_per_head_tile": round(1e3 * f_ms / head_tiles, 4),
+                        "bwd_us_per_head_tile": round(1e3 * w_ms / head_tiles, 4)})
+        per_config[label] = row
 
     # roofline of the dominant kernel (largest share of the timed region)
-    algo = {"attn_fwd": fwd_per_pair, "bwd_dkdv": 8.0 * D, "bwd_dq": 2.0 * D}
+    algo = {"attn_fwd": FWD_PER_PAIR, "bwd_dkdv": 8.0 * D, "bwd_dq": 2.0 * D}
     dom = max(prof.items(), key=lambda kv: kv[1][1])[0] if prof else None
     roofline = None
     if dom in algo:
         launches, ms = prof[dom]
-        achieved = algo[dom] * total_pairs / (ms * 1e-3) / 1e12
+        achieved = tflops(algo[dom] * total_pairs, ms)
         roofline = {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 1),
                     "peak": pk["bf16_sustained"], "unit": "TFLOP/s",
                     "frac": round(achieved / pk["bf16_sustained"], 4),
                     "frac_of_burst": round(achieved / pk["bf16"], 4),
                     "peak_note": f"{pk['source']} bf16 dense (sustained; burst {pk['bf16']})",
-                    "traffic": traffic_from_profiles(dom),
+                    "traffic": traffic_from_profiles(dom, tag),
                     "launches": launches, "avg_launch_ms": round(ms / launches, 3),
                     "algorithmic_flops_per_pair": algo[dom]}
     kernel_share = {k: round(v[1] / sum(x[1] for x in prof.values()), 4) for k, v in prof.items()}
     gpu_launches = int(sum(v[0] for v in prof.values()))
 
-    # ---- end to end through the public API with host buffers
-    e2e_steps = 0 if args.case else max(1, min(args.steps, 3))
-    h2d = {s: [x.pin_memory() for x in data[s]["host"]] for s in SEQLENS}
-    d2h = {s: [torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-               for t in (data[s]["o"], data[s]["lse"], data[s]["dq"], data[s]["dk"], data[s]["dv"])]
-           for s in SEQLENS}
-    h2d_bytes = sum(x.numel() * x.element_size() for s in SEQLENS for x in h2d[s])
-    d2h_bytes = sum(x.numel() * x.element_size() for s in SEQLENS for x in d2h[s])
-    e2e_ms, e2e_pairs = [], 0
-    for st in range(e2e_steps):
-        flush.zero_()
-        sync_all()
-        t0 = time.perf_counter()
-        pl = step(st, e2e={"h2d": h2d, "d2h": d2h})
-        sync_all()
-        e2e_ms.append(1e3 * (time.perf_counter() - t0))
-        e2e_pairs += sum(int(p.export()["n_valid"].sum()) * (HQ // p.info["map_heads"])
-                         for _, _, p in pl)
-    e2e_value = (world * e2e_pairs * (fwd_per_pair + bwd_per_pair) /
-                 (max_over_ranks(sum(e2e_ms)) * 1e-3) / 1e12) if e2e_steps else None
+    # ---- end to end through the public API with host buffers (default workload)
+    e2e_steps = max(1, min(args.steps, 3)) if default else 0
+    e2e_value, h2d_bytes, d2h_bytes = None, 0, 0
+    if e2e_steps:
+        h2d = [[x.pin_memory() for x in d["host"]] for d in data]
+        d2h = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                for t in (d["o"], d["lse"], d["dq"], d["dk"], d["dv"])] for d in data]
+        h2d_bytes = sum(x.numel() * x.element_size() for g in h2d for x in g)
+        d2h_bytes = sum(x.numel() * x.element_size() for g in d2h for x in g)
+        e2e_ms, e2e_pairs = [], 0
+        for st in range(e2e_steps):
+            flush.zero_()
+            sync_all()
+            t0 = time.perf_counter()
+            plans = step(st, e2e={"h2d": h2d, "d2h": d2h})
+            sync_all()
+            e2e_ms.append(1e3 * (time.perf_counter() - t0))
+            e2e_pairs += sum(c[2] for c in pair_counts(plans))
+            del plans
+        e2e_flops, e2e_total_ms = aggregate(e2e_pairs * (FWD_PER_PAIR + BWD_PER_PAIR),
+                                            sum(e2e_ms), dist, dev)
+        e2e_value = tflops(e2e_flops, e2e_total_ms)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        v, secs, what = oracle_sample(256, seed=0, budget_s=30.0)
+        v, secs, what = oracle_sample(groups, 256, seed=0, budget_s=30.0)
         cpu = {"value": v, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
                "sample": what + f" ({secs:.1f} s)"}
 
-    full_causal = [per_config[k] for k in per_config
-                   if k.split("/")[1] in ("FULL", "CAUSAL") and int(k[2:].split("/")[0]) >= 16384]
+    full_causal = [v for k, v in per_config.items()
+                   if k.split("/")[-1] in ("FULL", "CAUSAL") and int(k[2:].split("/")[0]) >= 16384]
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
@@ -395,10 +542,8 @@ def run_gpu(args, rank, world):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic: seeded N(0,1) bf16 Q/K/V/dO; lognormal document lengths (the "
                 "pages' corpora are not available)",
-        "config": {"workload": WORKLOAD if not args.case else f"single case {args.case}",
-                   "seqlens": list(SEQLENS),
-                   "masks": [m[0] for m in MASKS], "h_q": HQ, "h_kv": HKV, "head_dim": D,
-                   "batch_per_gpu": 1, "tiles": "128x128",
+        "config": {"workload": text, "suite": "case" if args.case else args.suite,
+                   "head_dim": D, "batch_per_gpu": 1, "tiles": "128x128",
                    "step": "per (S, mask): mask build + forward + backward",
                    "l2": "flushed before every timed step (256 MB write)",
                    "parallelism": f"replicas x{world} (independent batch entries, no collective)"},
@@ -410,9 +555,11 @@ def run_gpu(args, rank, world):
         "per_config": per_config,
         "roofline": roofline,
         "kernel_time_share": kernel_share,
+        "peak_memory_gb": round(peak_mem / 2**30, 3),
         "cpu_baseline": cpu,
-        "e2e": {"value": None if e2e_value is None else round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d_bytes,
-                "d2h_bytes_per_step": d2h_bytes, "steps": e2e_steps},
+        "e2e": {"value": None if e2e_value is None else round(e2e_value, 2), "unit": UNIT,
+                "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,
+                "steps": e2e_steps},
         "gpu_launches": gpu_launches,
         "clocks": clocks,
     }
@@ -429,19 +576,15 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--suite", choices=SUITES, default="dense",
+                    help="workload to time (default: the dense regular masks)")
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the timed oracle sample in the GPU arm")
     ap.add_argument("--case", default=None,
-                    help="run a single S:MASK case (e.g. 16384:FULL) for profiler captures; "
-                         "skips the end-to-end and CPU legs")
+                    help="run a single S:MASK case of the dense workload (e.g. 16384:FULL) "
+                         "for profiler captures; skips the end-to-end and CPU legs")
     args = ap.parse_args()
     if args.case:
-        global SEQLENS, MASKS
-        s_txt, m_txt = args.case.split(":")
-        SEQLENS = (int(s_txt),)
-        MASKS = tuple(m for m in MASKS if m[0] == m_txt)
-        if not MASKS:
-            ap.error(f"unknown mask {m_txt}")
         args.no_cpu_baseline = True
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -150,6 +150,13 @@ class Plan:
         out["cls"] = out["cls"].reshape(hm, nq, nk)
         return out
 
+    def n_valid(self) -> np.ndarray:
+        """Allowed (i, j) pairs per map head (int64 [map_heads]); copies nothing else."""
+        nv = np.zeros(self.info["map_heads"], np.int64)
+        _check("lca_plan_export", load_library().lca_plan_export(
+            self._h, *([None] * 9), nv.ctypes.data_as(ctypes.c_void_p)))
+        return nv
+
     def __del__(self):
         if getattr(self, "_h", None) is not None and self._h.value and _lib is not None:
             _lib.lca_plan_destroy(self._h)
