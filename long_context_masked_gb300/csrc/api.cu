@@ -419,6 +419,9 @@ AttnDims make_dims(const lca_plan* p, const lca_shape* s, float softmax_scale) {
   d.kv_per_map = p->info.map_heads <= s->h_kv ? s->h_kv / p->info.map_heads : 0;
   d.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(s->head_dim));
   d.scale_log2 = d.scale * 1.4426950408889634f;
+  // 16 consecutive work items per launch-order group: MHA kernels then share K/V
+  // (Q/dO) tiles in L2 across the resident CTAs; GQA is indifferent to it.
+  d.chunk = 16;
   return d;
 }
 

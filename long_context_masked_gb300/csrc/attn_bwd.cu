@@ -208,8 +208,8 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   int b, hk, kt;
   if (dm.kv_per_map > 0) {
     const int per_item = dm.kv_per_map * dm.batch;
-    const int item = blockIdx.x / per_item;
-    const int rem = blockIdx.x - item * per_item;
+    int item, rem;
+    chunked_item(blockIdx.x, per_item, pl.map_heads * pl.n_kt, dm.chunk, item, rem);
     const int col = __ldg(pl.work_k + item);
     const int hm = col / pl.n_kt;
     kt = col - hm * pl.n_kt;
@@ -419,6 +419,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       }
     };
     if (have) load_rows(h, qt);
+    MapCursor mcur;
     while (have) {
       const int i = qt * BM + row;
       const bool valid = i < S;
@@ -428,7 +429,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       uint32_t bits[2] = {0u, 0u};
       if (masked && valid) {
         const RowSpan sp = row_span(a.mask, i);
-        row_tile_bits<2>(a.mask, h / dm.heads_per_map, i, c0, sp, bits);
+        row_tile_bits<2>(a.mask, h / dm.heads_per_map, i, c0, sp, bits, &mcur);
       }
       int h_n, qt_n, cls_n;
       const bool have_n = walk.next(h_n, qt_n, cls_n);
@@ -518,8 +519,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   const int S = dm.seqlen;
 
   const int per_item = dm.heads_per_map * dm.batch;
-  const int item = blockIdx.x / per_item;
-  const int rem = blockIdx.x - item * per_item;
+  int item, rem;
+  chunked_item(blockIdx.x, per_item, pl.map_heads * pl.n_qt, dm.chunk, item, rem);
   const int row = __ldg(pl.work_q + item);
   const int hm = row / pl.n_qt;
   const int qt = row - hm * pl.n_qt;
@@ -683,12 +684,13 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       dsum = __ldg(a.dsum + rowi);
     }
     const RowSpan sp = row_span(a.mask, min(i, S - 1));
+    MapCursor mcur;
     for (int n = 0; n < n_tiles; ++n) {
       const int kt = __ldg(pl.kt_idx + beg + n);
       const int cls = __ldg(pl.kt_cls + beg + n);
       const bool masked = cls != LCA_TILE_FULL || kt * BN + BN > S || qt * BM + BM > S;
       uint32_t bits[2] = {0u, 0u};
-      if (masked && valid) row_tile_bits<2>(a.mask, hm, i, kt * BN + half * 64, sp, bits);
+      if (masked && valid) row_tile_bits<2>(a.mask, hm, i, kt * BN + half * 64, sp, bits, &mcur);
       mbar_wait(&bar.sdp_full, n & 1, wc);
       __syncwarp();
       tc_fence_after();

@@ -95,8 +95,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   const AttnDims& dm = a.dims;
   const PlanDev& pl = a.plan;
   const int per_item = dm.heads_per_map * dm.batch;
-  const int item = blockIdx.x / per_item;
-  const int rem = blockIdx.x - item * per_item;
+  int item, rem;
+  chunked_item(blockIdx.x, per_item, pl.map_heads * pl.n_qt, dm.chunk, item, rem);
   const int sub = rem % dm.heads_per_map;
   const int b = rem / dm.heads_per_map;
   const int row = __ldg(pl.work_q + item);
@@ -238,6 +238,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const uint32_t quarter_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const uint32_t lane_addr = quarter_addr + half * 64;
     const RowSpan sp = row_span(a.mask, min(i, S - 1));
+    MapCursor mcur;
     const float sl2 = dm.scale_log2;
     float* red = reinterpret_cast<float*>(base + OFF_RED);  // [parity][half][row]
     float m_run = -INFINITY;
@@ -252,7 +253,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       const int c0 = kt * BN + half * 64;
       const bool masked = cls != LCA_TILE_FULL || kt * BN + BN > S;
       uint32_t bits[2] = {0u, 0u};
-      if (masked && i < S) row_tile_bits<2>(a.mask, hm, i, c0, sp, bits);
+      if (masked && i < S) row_tile_bits<2>(a.mask, hm, i, c0, sp, bits, &mcur);
       mbar_wait(&bar.s_full[st], ph, wc);
       __syncwarp();
       tc_fence_after();

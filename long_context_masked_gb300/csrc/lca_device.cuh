@@ -327,6 +327,23 @@ __device__ __forceinline__ uint32_t sw128_offset(uint32_t r, uint32_t u) {
 
 // ------------------------------------------------------------------ masks
 
+// Launch order of the per-head CTAs of a work list.  CTA blk maps to work item `item`
+// (an index into the longest-first list) and replica `rem` (query or KV head within
+// the map head, times batch).  The replicas of `chunk` consecutive items are
+// interleaved item-fastest, so the CTAs resident at one time cover several items of
+// the same head: for MHA they then stream the same K/V (or Q/dO) tiles together and
+// share them in L2, where head-fastest order would give every CTA its own stream.
+__device__ __forceinline__ void chunked_item(int blk, int per_item, int n_items, int chunk,
+                                             int& item, int& rem) {
+  const int span = chunk * per_item;
+  const int c = blk / span;
+  const int first = c * chunk;
+  const int cn = min(chunk, n_items - first);
+  const int w = blk - c * span;
+  item = first + w % cn;
+  rem = w / cn;
+}
+
 // Index s of the segment [cu[s], cu[s+1]) holding x, for 0 <= x < cu[n].
 __device__ __forceinline__ int seg_find(const int32_t* cu, int n, int x) {
   int lo = 0, hi = n - 1;
@@ -336,6 +353,29 @@ __device__ __forceinline__ int seg_find(const int32_t* cu, int n, int x) {
   }
   return lo;
 }
+
+// seg_find for an ascending x sequence: starts at `hint` (any index; the answer from
+// the previous, smaller x) and gallops upward, so a cursor that moves by a few blocks
+// costs a few loads.  Falls back to the full search when the hint is past x.
+__device__ __forceinline__ int seg_find_from(const int32_t* cu, int n, int hint, int x) {
+  if (hint < 0 || hint >= n || __ldg(cu + hint) > x) return seg_find(cu, n, x);
+  int lo = hint, step = 1;
+  while (lo + step <= n - 1 && __ldg(cu + lo + step) <= x) {
+    lo += step;
+    step <<= 1;
+  }
+  int hi = min(n - 1, lo + step - 1);
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(cu + mid) <= x) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Per-thread search hints of the variable block-sparse map: the row block of the last
+// row and the column block of the last column window looked up.  Only speed depends
+// on them; start them at -1.
+struct MapCursor { int rb = -1, cb = -1; };
 
 // Allowed keys of query row i as two disjoint half-open intervals inside [0, S):
 // [a0, b0) and [a1, b1) (either may be empty).  Block-sparse masks return their base
@@ -428,7 +468,8 @@ __device__ __forceinline__ uint32_t range_bits(int lo, int hi, int ws) {
 // column c0 + 32w + c).  Columns >= S are never allowed.
 template <int NW>
 __device__ __forceinline__ void row_tile_bits(const MaskDev& m, int h_m, int i, int c0,
-                                              const RowSpan& sp, uint32_t (&bits)[NW]) {
+                                              const RowSpan& sp, uint32_t (&bits)[NW],
+                                              MapCursor* cur = nullptr) {
 #pragma unroll
   for (int w = 0; w < NW; ++w)
     bits[w] = range_bits(sp.a0, sp.b0, c0 + 32 * w) | range_bits(sp.a1, sp.b1, c0 + 32 * w);
@@ -450,9 +491,16 @@ __device__ __forceinline__ void row_tile_bits(const MaskDev& m, int h_m, int i, 
   } else {
     const int32_t* ro = m.row_off + static_cast<size_t>(h_m) * (m.n_rb + 1);
     const int32_t* co = m.col_off + static_cast<size_t>(h_m) * (m.n_cb + 1);
-    const int rb = seg_find(ro, m.n_rb, i);
+    int rb, cb0;
+    if (cur != nullptr) {
+      rb = cur->rb = seg_find_from(ro, m.n_rb, cur->rb, i);
+      cb0 = cur->cb = seg_find_from(co, m.n_cb, cur->cb, c0);
+    } else {
+      rb = seg_find(ro, m.n_rb, i);
+      cb0 = seg_find(co, m.n_cb, c0);
+    }
     const uint8_t* row = m.bmap + (static_cast<size_t>(h_m) * m.n_rb + rb) * m.n_cb;
-    for (int cb = seg_find(co, m.n_cb, c0); cb < m.n_cb; ++cb) {
+    for (int cb = cb0; cb < m.n_cb; ++cb) {
       const int lo = __ldg(co + cb);
       if (lo >= c1) break;
       if (__ldg(row + cb)) {

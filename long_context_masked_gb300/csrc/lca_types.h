@@ -44,6 +44,7 @@ struct AttnDims {
                                         // and a KV group spans several maps)
   float scale;                          // softmax scale
   float scale_log2;                     // scale * log2(e)
+  int chunk;                            // work items interleaved per launch-order group
 };
 
 }  // namespace lca

@@ -14,6 +14,8 @@
 // restricted by the block map for the sparse masks), so no S x S mask is ever built.
 #include <cuda_runtime.h>
 
+#include <climits>
+
 #include "lca_device.cuh"
 #include "mask_build.h"
 
@@ -39,6 +41,7 @@ __global__ void __launch_bounds__(TQ) classify_kernel(MaskDev m, int n_qt, int n
   __shared__ unsigned long long s_red[NWARP];
   __shared__ int s_len[NWARP];
   __shared__ int s_part[NWARP];
+  __shared__ int s_lo[NWARP], s_hi[NWARP];
 
   const int qt = blockIdx.x, hm = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -49,6 +52,25 @@ __global__ void __launch_bounds__(TQ) classify_kernel(MaskDev m, int n_qt, int n
   if (valid) sp = row_span(m, i);
   const bool sparse = is_sparse(m.type);
 
+  // Key tiles outside the hull of the block's allowed intervals are SKIP without any
+  // per-row work (documents and windows leave most of a long row's tiles there).
+  int lo = INT_MAX, hi = 0;
+  if (valid) {
+    if (sp.a0 < sp.b0) { lo = sp.a0; hi = sp.b0; }
+    if (sp.a1 < sp.b1) { lo = min(lo, sp.a1); hi = max(hi, sp.b1); }
+  }
+  for (int off = 16; off > 0; off >>= 1) {
+    lo = min(lo, __shfl_xor_sync(0xFFFFFFFFu, lo, off));
+    hi = max(hi, __shfl_xor_sync(0xFFFFFFFFu, hi, off));
+  }
+  if (lane == 0) { s_lo[warp] = lo; s_hi[warp] = hi; }
+  __syncthreads();
+#pragma unroll
+  for (int w = 0; w < NWARP; ++w) { lo = min(lo, s_lo[w]); hi = max(hi, s_hi[w]); }
+  const int kt_lo = lo == INT_MAX ? n_kt : lo / TK;
+  const int kt_hi = lo == INT_MAX ? n_kt : (hi + TK - 1) / TK;
+  MapCursor mcur;
+
   unsigned long long my_count = 0;
   int my_len = 0, my_part = 0;
   uint8_t* cls_row = cls + (static_cast<size_t>(hm) * n_qt + qt) * n_kt;
@@ -56,13 +78,20 @@ __global__ void __launch_bounds__(TQ) classify_kernel(MaskDev m, int n_qt, int n
   for (int k0 = 0; k0 < n_kt; k0 += KT_CHUNK) {
     const int k1 = min(n_kt, k0 + KT_CHUNK);
     for (int kt = k0; kt < k1; ++kt) {
+      if (kt < kt_lo || kt >= kt_hi) {  // block-uniform
+        if (lane == 0) {
+          s_any[warp][kt - k0] = 0;
+          s_all[warp][kt - k0] = 0;
+        }
+        continue;
+      }
       const int c0 = kt * TK;
       const int width = min(TK, S - c0);
       int cnt = 0;
       if (valid) {
         if (sparse) {
           uint32_t bits[NW];
-          row_tile_bits<NW>(m, hm, i, c0, sp, bits);
+          row_tile_bits<NW>(m, hm, i, c0, sp, bits, &mcur);
 #pragma unroll
           for (int w = 0; w < NW; ++w) cnt += __popc(bits[w]);
         } else {
