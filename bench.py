@@ -362,7 +362,9 @@ def run_gpu(args, rank, world):
                      "dq": torch.empty((1, s, hq, D), dtype=torch.bfloat16, device=dev),
                      "dk": torch.empty((1, s, hkv, D), dtype=torch.bfloat16, device=dev),
                      "dv": torch.empty((1, s, hkv, D), dtype=torch.bfloat16, device=dev),
-                     "ws": torch.empty((hq * s,), dtype=torch.float32, device=dev)})
+                     # lca_attn_bwd_workspace: LSE2 and D rows padded to 128
+                     "ws": torch.empty((2 * hq * ((s + 127) // 128 * 128),),
+                                       dtype=torch.float32, device=dev)})
         del q, k, v, do
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()

@@ -169,7 +169,9 @@ lca_status lca_attn_fwd(const lca_plan* plan, const lca_shape* shape, const void
                         const void* k, const void* v, void* o, float* lse, float softmax_scale,
                         void* stream);
 
-/* Bytes of device workspace lca_attn_bwd needs (D = rowsum(dO * O), fp32). */
+/* Bytes of device workspace lca_attn_bwd needs: two fp32 rows per (batch, query head),
+ * LSE * log2(e) and D = rowsum(dO * O), each padded to seqlen rounded up to 128, i.e.
+ * 8 * batch * h_q * round_up(seqlen, 128) bytes (0 for a NULL plan or shape). */
 size_t lca_attn_bwd_workspace(const lca_plan* plan, const lca_shape* shape, int flags);
 
 /* Backward: dQ, dK, dV (bf16) from Q, K, V, O, dO and the forward's LSE.
@@ -188,9 +190,10 @@ lca_status lca_attn_bwd(const lca_plan* plan, const lca_shape* shape, const void
  * workspace of lca_attn_bwd comes from.
  *
  * Same arguments, preconditions and results as lca_attn_bwd (flags 0), except that
- * the D workspace is a fixed 32 MiB buffer compiled into the library (a file-scope
+ * the workspace is a fixed 64 MiB buffer compiled into the library (a file-scope
  * device array that every GPU loading the library holds until the process exits),
- * so it serves at most batch * h_q * seqlen <= 2^23 rows; larger shapes return
+ * so it serves at most batch * h_q * round_up(seqlen, 128) <= 2^23 rows; larger
+ * shapes return
  * LCA_ERR_UNSUPPORTED without launching anything.  No cudaMalloc / cudaFree is made
  * (with lca_profile_enable on, the timing events of the launches come from a pool
  * that grows on first use).

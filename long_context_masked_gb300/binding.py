@@ -253,7 +253,7 @@ def attn_bwd_noalloc(plan: Plan, q, k, v, o, do, lse, scale: Optional[float] = N
                      dk=None, dv=None, stream=None):
     """dQ, dK, dV through lca_attn_bwd_noalloc: the backward for callers that cannot
     allocate device memory at that point; its workspace is the library's fixed
-    built-in buffer (batch * h_q * seqlen <= 2^23).  Pass preallocated dq/dk/dv to
+    built-in buffer (batch * h_q * round_up(seqlen, 128) <= 2^23).  Pass preallocated dq/dk/dv to
     keep the call free of allocations on the Python side too."""
     import torch
 

@@ -408,6 +408,8 @@ lca_status check_shape(const lca_plan* p, const lca_shape* s) {
   return LCA_OK;
 }
 
+int64_t padded_seqlen(int seqlen) { return (static_cast<int64_t>(seqlen) + 127) / 128 * 128; }
+
 AttnDims make_dims(const lca_plan* p, const lca_shape* s, float softmax_scale) {
   AttnDims d;
   d.batch = s->batch;
@@ -460,8 +462,10 @@ lca_status lca_attn_fwd(const lca_plan* plan, const lca_shape* shape, const void
 
 size_t lca_attn_bwd_workspace(const lca_plan* plan, const lca_shape* shape, int flags) {
   (void)flags;
-  if (!plan || !shape) return 0;
-  return static_cast<size_t>(shape->batch) * shape->h_q * shape->seqlen * sizeof(float);
+  if (!plan || !shape || shape->batch < 1 || shape->h_q < 1 || shape->seqlen < 1) return 0;
+  // LSE2 and D rows, each padded to whole 128-row tiles
+  return 2 * static_cast<size_t>(shape->batch) * shape->h_q * padded_seqlen(shape->seqlen) *
+         sizeof(float);
 }
 
 lca_status lca_attn_bwd(const lca_plan* plan, const lca_shape* shape, const void* q,
@@ -490,7 +494,9 @@ lca_status lca_attn_bwd(const lca_plan* plan, const lca_shape* shape, const void
   a.o = static_cast<const __nv_bfloat16*>(o);
   a.dout = static_cast<const __nv_bfloat16*>(dout);
   a.lse = lse;
-  a.dsum = static_cast<float*>(workspace);
+  a.s_pad = padded_seqlen(shape->seqlen);
+  a.lse2 = static_cast<float*>(workspace);
+  a.dsum = a.lse2 + static_cast<size_t>(shape->batch) * shape->h_q * a.s_pad;
   a.dq = static_cast<__nv_bfloat16*>(dq);
   a.dk = static_cast<__nv_bfloat16*>(dk);
   a.dv = static_cast<__nv_bfloat16*>(dv);

@@ -39,15 +39,19 @@ constexpr float LOG2E = 1.4426950408889634f;
 // ------------------------------------------------------------------ preprocess
 
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(BwdArgs a) {
+  // One 16-thread group per (b, i, h) row of the padded workspace, h fastest so the O
+  // and dO reads coalesce; rows i >= S only write the padding values.
   const int S = a.dims.seqlen, hq = a.dims.h_q;
-  const int64_t rows = static_cast<int64_t>(a.dims.batch) * S * hq;
+  const int64_t rows = static_cast<int64_t>(a.dims.batch) * a.s_pad * hq;
   const int64_t r = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 4;
   const int part = threadIdx.x & 15;
+  const int h = static_cast<int>(r % hq);
+  const int64_t bi = r / hq;
+  const int64_t b = bi / a.s_pad, i = bi % a.s_pad;
+  const bool live = r < rows && i < S;
   float acc = 0.f;
-  if (r < rows) {
-    const int h = static_cast<int>(r % hq);
-    const int64_t bi = r / hq;
-    const int64_t off = bi * a.o_row_stride + h * HD + part * 8;
+  if (live) {
+    const int64_t off = (b * S + i) * a.o_row_stride + h * HD + part * 8;
     const uint4 ov = *reinterpret_cast<const uint4*>(a.o + off);
     const uint4 gv = *reinterpret_cast<const uint4*>(a.dout + off);
     const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
@@ -63,10 +67,14 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(BwdArgs a) {
 #pragma unroll
   for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
   if (part == 0 && r < rows) {
-    const int h = static_cast<int>(r % hq);
-    const int64_t bi = r / hq;
-    const int64_t b = bi / S, i = bi % S;
-    a.dsum[(b * hq + h) * S + i] = acc;
+    const int64_t w = (b * hq + h) * a.s_pad + i;
+    float l2 = INFINITY;
+    if (live) {
+      const float l = a.lse[(b * hq + h) * S + i];
+      if (l != -INFINITY) l2 = l * LOG2E;
+    }
+    a.dsum[w] = acc;
+    a.lse2[w] = l2;
   }
 }
 
@@ -134,31 +142,50 @@ __device__ __forceinline__ void store_acc_half(uint32_t taddr, bool have, float 
   }
 }
 
-__device__ __forceinline__ uint8_t* aligned_smem(uint8_t* raw, uint32_t& base_u32) {
-  const uint32_t raw_u32 = smem_u32(raw);
-  base_u32 = (raw_u32 + 1023u) & ~1023u;
-  return raw + (base_u32 - raw_u32);
-}
-
 // ------------------------------------------------------------------ dK / dV
+//
+// Key-major orientation: the CTA's 128 key rows are the TMEM lanes, so
+//   S^T = K Q^T, dP^T = V dO^T           SS MMAs, both operands K-major, N = 128
+//   P^T = exp2(S^T scale_log2 - LSE2),   dS^T = P^T (dP^T - D)
+//   dV += P^T dO, dK += dS^T Q           TS MMAs: P^T / dS^T from TMEM, dO / Q MN-major
+// A softmax thread owns one key row and 64 query columns; it writes P^T (dS^T) back as
+// bf16 pairs into the first 32 of its own 64 S^T (dP^T) columns, so P and dS never pass
+// through shared memory.  The next S^T (dP^T) overwrites P^T (dS^T), so it is issued
+// once dV (dK) of the previous step completed; the issue order dV(t), dK(t), S^T(t+1),
+// dP^T(t+1) keeps the tensor pipe fed across those waits.  LSE2 = LSE log2(e) and D of
+// the step's 128 queries arrive in shared memory with the Q and dO tiles (bulk copies
+// from the padded workspace rows).  Both stages are released when dK completes (the
+// softmax reads D until it hands over dS^T); Q gets three stages, dO two.
 
+constexpr int KV_QST = 3;
+constexpr int KV_DOST = 2;
+constexpr uint32_t ROWV = BM * 4;                   // one step's LSE2 or D values
 constexpr uint32_t KV_OFF_K = 0;
 constexpr uint32_t KV_OFF_V = TILE;
-constexpr uint32_t KV_OFF_Q = 2 * TILE;        // 2 stages
-constexpr uint32_t KV_OFF_DO = 4 * TILE;       // 2 stages
-constexpr uint32_t KV_OFF_PDS = 6 * TILE;
-constexpr uint32_t KV_OFF_BAR = 7 * TILE;
-constexpr uint32_t KV_SMEM = KV_OFF_BAR + 256 + 1024;
+constexpr uint32_t KV_OFF_Q = 2 * TILE;
+constexpr uint32_t KV_OFF_DO = KV_OFF_Q + KV_QST * TILE;
+constexpr uint32_t KV_OFF_LSE = KV_OFF_DO + KV_DOST * TILE;   // one per Q stage
+constexpr uint32_t KV_OFF_D = KV_OFF_LSE + KV_QST * ROWV;     // one per dO stage
+constexpr uint32_t KV_OFF_BAR = KV_OFF_D + KV_DOST * ROWV;
+constexpr uint32_t KV_SMEM = KV_OFF_BAR + 256;                // the dynamic base is 1024-aligned
 static_assert(KV_SMEM <= 232448, "dynamic shared memory above the 227 KB per-CTA limit");
 constexpr uint32_t KV_TM_S = 0, KV_TM_DP = 128, KV_TM_DV = 256, KV_TM_DK = 384;
 
 struct KvBars {
   uint64_t kv_full;
-  uint64_t q_full[2], q_empty[2], do_full[2], do_empty[2];
-  uint64_t sdp_full, sdp_free, p_ready, dv_done, ds_ready, dk_done;
+  uint64_t q_full[KV_QST], q_empty[KV_QST], do_full[KV_DOST], do_empty[KV_DOST];
+  uint64_t s_full, dp_full, p_ready, ds_ready, dv_done, dk_done;
   uint32_t tmem_base;
   int abort;
 };
+static_assert(sizeof(KvBars) <= 256, "barrier block overflows its shared-memory slot");
+
+// TMEM column of the bf16 pairs of queries [16 kk, 16 kk + 16) in a P^T / dS^T region:
+// queries 0-63 sit in columns 0-31 (written by the half-0 threads), queries 64-127 in
+// columns 64-95 (half 1), each inside the columns its writer has already read.
+__host__ __device__ constexpr uint32_t kv_pair_col(int kk) {
+  return kk < 4 ? kk * 8 : 64 + (kk - 4) * 8;
+}
 
 // Walks the (query head, query tile) pairs feeding one key tile: every query head of
 // the KV group, each with the transposed list of its map head (head-major: measured
@@ -196,9 +223,13 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
 bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                 BwdArgs a) {
-  extern __shared__ uint8_t smem_raw[];
-  uint32_t base_u32;
-  uint8_t* base = aligned_smem(smem_raw, base_u32);
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t base_u32 = smem_u32(smem_raw);
+  if (base_u32 & 1023u) {
+    if (threadIdx.x == 0) atomicOr(a.err, LCA_DEVERR_LAYOUT);
+    return;
+  }
+  uint8_t* base = smem_raw;
   KvBars& bar = *reinterpret_cast<KvBars*>(base + KV_OFF_BAR);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const AttnDims& dm = a.dims;
@@ -224,17 +255,19 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
   if (threadIdx.x == 0) {
     mbar_init(&bar.kv_full, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < KV_QST; ++s) {
       mbar_init(&bar.q_full[s], 1);
       mbar_init(&bar.q_empty[s], 1);
+    }
+    for (int s = 0; s < KV_DOST; ++s) {
       mbar_init(&bar.do_full[s], 1);
       mbar_init(&bar.do_empty[s], 1);
     }
-    mbar_init(&bar.sdp_full, 1);
-    mbar_init(&bar.sdp_free, SOFTMAX_THREADS);
+    mbar_init(&bar.s_full, 1);
+    mbar_init(&bar.dp_full, 1);
     mbar_init(&bar.p_ready, SOFTMAX_THREADS);
-    mbar_init(&bar.dv_done, 1);
     mbar_init(&bar.ds_ready, SOFTMAX_THREADS);
+    mbar_init(&bar.dv_done, 1);
     mbar_init(&bar.dk_done, 1);
     bar.abort = 0;
     fence_mbar_init();
@@ -250,226 +283,229 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   WaitCtx wc{&bar.abort, a.err, a.timeout_ns};
   ColWalk walk;
   walk.init(&pl, kt, hk, dm);
+  const int64_t row0 = static_cast<int64_t>(b) * dm.h_q;   // workspace row of head 0
 
   if (warp == WARP_PRODUCER) {
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_do);
       mbar_arrive_expect_tx(&bar.kv_full, 2 * TILE);
       for (int c = 0; c < 2; ++c) {
         tma_load_4d(base + KV_OFF_K + c * HALF, &tm_k, &bar.kv_full, c * 64, hk, kt * BN, b);
         tma_load_4d(base + KV_OFF_V + c * HALF, &tm_v, &bar.kv_full, c * 64, hk, kt * BN, b);
       }
       int h, qt, cls, t = 0;
-      ColWalk ahead = walk;   // two steps ahead: L2 prefetch of the Q tile
+      ColWalk ahead = walk;   // L2 prefetch of the Q tile KV_QST steps ahead
       int ha, qa, ca;
-      for (int k = 0; k < 2 && ahead.next(ha, qa, ca); ++k)
+      for (int k = 0; k < KV_QST && ahead.next(ha, qa, ca); ++k)
         for (int c = 0; c < 2; ++c) tma_prefetch_l2_4d(&tm_q, c * 64, ha, qa * BM, b);
       while (walk.next(h, qt, cls)) {
-        const int st = t & 1;
-        const uint32_t ph = (t >> 1) & 1;
+        const int st = t % KV_QST;
+        const uint32_t ph = (t / KV_QST) & 1;
         if (ahead.next(ha, qa, ca))
           for (int c = 0; c < 2; ++c) tma_prefetch_l2_4d(&tm_q, c * 64, ha, qa * BM, b);
-        if (t >= 2) mbar_wait(&bar.q_empty[st], ph ^ 1u, wc);
-        mbar_arrive_expect_tx(&bar.q_full[st], TILE);
+        if (t >= KV_QST) mbar_wait(&bar.q_empty[st], ph ^ 1u, wc);
+        mbar_arrive_expect_tx(&bar.q_full[st], TILE + ROWV);
         for (int c = 0; c < 2; ++c)
           tma_load_4d(base + KV_OFF_Q + st * TILE + c * HALF, &tm_q, &bar.q_full[st], c * 64, h,
                       qt * BM, b);
+        bulk_load(base + KV_OFF_LSE + st * ROWV,
+                  a.lse2 + (row0 + h) * a.s_pad + static_cast<int64_t>(qt) * BM, ROWV,
+                  &bar.q_full[st]);
         ++t;
       }
       if (bar.abort) {
         mbar_wait_final(&bar.kv_full, 0, a.timeout_ns);
-        for (int n = max(0, t - 2); n < t; ++n)
-          mbar_wait_final(&bar.q_full[n & 1], (n >> 1) & 1, a.timeout_ns);
+        for (int n = max(0, t - KV_QST); n < t; ++n)
+          mbar_wait_final(&bar.q_full[n % KV_QST], (n / KV_QST) & 1, a.timeout_ns);
       }
     }
   } else if (warp == WARP_PRODUCER_2) {
-    // dO stages are freed by dV, earlier than Q stages (freed by dK): a separate warp
-    // refills them without queueing behind the Q releases
     if (lane == 0) {
+      tma_prefetch_desc(&tm_do);
       int h, qt, cls, t = 0;
-      ColWalk ahead = walk;   // two steps ahead: L2 prefetch of the dO tile
+      ColWalk ahead = walk;   // L2 prefetch of the dO tile KV_QST steps ahead
       int ha, qa, ca;
-      for (int k = 0; k < 2 && ahead.next(ha, qa, ca); ++k)
+      for (int k = 0; k < KV_QST && ahead.next(ha, qa, ca); ++k)
         for (int c = 0; c < 2; ++c) tma_prefetch_l2_4d(&tm_do, c * 64, ha, qa * BM, b);
       while (walk.next(h, qt, cls)) {
-        const int st = t & 1;
-        const uint32_t ph = (t >> 1) & 1;
+        const int st = t % KV_DOST;
+        const uint32_t ph = (t / KV_DOST) & 1;
         if (ahead.next(ha, qa, ca))
           for (int c = 0; c < 2; ++c) tma_prefetch_l2_4d(&tm_do, c * 64, ha, qa * BM, b);
-        if (t >= 2) mbar_wait(&bar.do_empty[st], ph ^ 1u, wc);
-        mbar_arrive_expect_tx(&bar.do_full[st], TILE);
+        if (t >= KV_DOST) mbar_wait(&bar.do_empty[st], ph ^ 1u, wc);
+        mbar_arrive_expect_tx(&bar.do_full[st], TILE + ROWV);
         for (int c = 0; c < 2; ++c)
-          tma_load_4d(base + KV_OFF_DO + st * TILE + c * HALF, &tm_do, &bar.do_full[st], c * 64, h,
-                      qt * BM, b);
+          tma_load_4d(base + KV_OFF_DO + st * TILE + c * HALF, &tm_do, &bar.do_full[st], c * 64,
+                      h, qt * BM, b);
+        bulk_load(base + KV_OFF_D + st * ROWV,
+                  a.dsum + (row0 + h) * a.s_pad + static_cast<int64_t>(qt) * BM, ROWV,
+                  &bar.do_full[st]);
         ++t;
       }
       if (bar.abort) {
-        for (int n = max(0, t - 2); n < t; ++n)
-          mbar_wait_final(&bar.do_full[n & 1], (n >> 1) & 1, a.timeout_ns);
+        for (int n = max(0, t - KV_DOST); n < t; ++n)
+          mbar_wait_final(&bar.do_full[n % KV_DOST], (n / KV_DOST) & 1, a.timeout_ns);
       }
     }
   } else if (warp == WARP_MMA) {
     if (lane == 0) {
-      constexpr uint32_t IDESC_NT = idesc_bf16(BM, BN, 0, 0);  // S, dP
-      constexpr uint32_t IDESC_TT = idesc_bf16(BN, HD, 1, 1);  // dV, dK (A, B MN-major)
+      constexpr uint32_t IDESC_SS = idesc_bf16(BN, BM, 0, 0);  // S^T, dP^T
+      constexpr uint32_t IDESC_TS = idesc_bf16(BN, HD, 0, 1);  // dV, dK (B MN-major)
       const uint64_t dk_ = desc_kmajor(base_u32 + KV_OFF_K, 0, HALF);
       const uint64_t dv_ = desc_kmajor(base_u32 + KV_OFF_V, 0, HALF);
       const uint64_t dq_k0 = desc_kmajor(base_u32 + KV_OFF_Q, 0, HALF);
       const uint64_t ddo_k0 = desc_kmajor(base_u32 + KV_OFF_DO, 0, HALF);
       const uint64_t dq_m0 = desc_mnmajor(base_u32 + KV_OFF_Q, 0, HALF);
       const uint64_t ddo_m0 = desc_mnmajor(base_u32 + KV_OFF_DO, 0, HALF);
-      const uint64_t dpds = desc_mnmajor(base_u32 + KV_OFF_PDS, 0, HALF);
       int total = 0;
       {
         ColWalk w2 = walk;
         int h, qt, cls;
         while (w2.next(h, qt, cls)) ++total;
       }
-      // Three MMA groups per (head, query tile) step t: SdP(t) = {S, dP}, dV(t), dK(t).
-      // They are issued as soon as their inputs are ready rather than in a fixed order, so
-      // a late Q/dO tile for SdP(t+1) never holds back dV(t) or dK(t).  Barrier phases
-      // cannot run ahead of the tests below: SdP(t+1) needs the softmax's release of
-      // S/dP(t); the softmax writes P(t+1) only after dK(t) completed, so p_ready and
-      // ds_ready are at most one phase beyond the step they are tested for.
-      auto issue_sdp = [&](int t) {
-        const int st = t & 1;
-        const uint64_t dq = dq_k0 + st * stage_step(TILE);
-        const uint64_t ddo = ddo_k0 + st * stage_step(TILE);
+      auto issue_s = [&](int t) {
+        const uint64_t dq = dq_k0 + (t % KV_QST) * stage_step(TILE);
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk)
-          umma_bf16_ss(tmem + KV_TM_S, dq + kmajor_step(kk, HALF), dk_ + kmajor_step(kk, HALF),
-                       IDESC_NT, kk > 0 ? 1u : 0u);
+          umma_bf16_ss(tmem + KV_TM_S, dk_ + kmajor_step(kk, HALF), dq + kmajor_step(kk, HALF),
+                       IDESC_SS, kk > 0 ? 1u : 0u);
+        umma_commit(&bar.s_full);
+      };
+      auto issue_dp = [&](int t) {
+        const uint64_t ddo = ddo_k0 + (t % KV_DOST) * stage_step(TILE);
+        tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk)
-          umma_bf16_ss(tmem + KV_TM_DP, ddo + kmajor_step(kk, HALF), dv_ + kmajor_step(kk, HALF),
-                       IDESC_NT, kk > 0 ? 1u : 0u);
-        umma_commit(&bar.sdp_full);
+          umma_bf16_ss(tmem + KV_TM_DP, dv_ + kmajor_step(kk, HALF), ddo + kmajor_step(kk, HALF),
+                       IDESC_SS, kk > 0 ? 1u : 0u);
+        umma_commit(&bar.dp_full);
       };
       auto issue_dv = [&](int t) {
-        const int st = t & 1;
-        const uint64_t ddo = ddo_m0 + st * stage_step(TILE);
+        const uint64_t ddo = ddo_m0 + (t % KV_DOST) * stage_step(TILE);
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BM / 16; ++kk)
-          umma_bf16_ss(tmem + KV_TM_DV, dpds + mnmajor_step(kk), ddo + mnmajor_step(kk),
-                       IDESC_TT, (t > 0 || kk > 0) ? 1u : 0u);
+          umma_bf16_ts(tmem + KV_TM_DV, tmem + KV_TM_S + kv_pair_col(kk), ddo + mnmajor_step(kk),
+                       IDESC_TS, (t > 0 || kk > 0) ? 1u : 0u);
         umma_commit(&bar.dv_done);
-        umma_commit(&bar.do_empty[st]);
       };
       auto issue_dk = [&](int t) {
-        const int st = t & 1;
+        const int st = t % KV_QST;
         const uint64_t dq = dq_m0 + st * stage_step(TILE);
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BM / 16; ++kk)
-          umma_bf16_ss(tmem + KV_TM_DK, dpds + mnmajor_step(kk), dq + mnmajor_step(kk),
-                       IDESC_TT, (t > 0 || kk > 0) ? 1u : 0u);
+          umma_bf16_ts(tmem + KV_TM_DK, tmem + KV_TM_DP + kv_pair_col(kk), dq + mnmajor_step(kk),
+                       IDESC_TS, (t > 0 || kk > 0) ? 1u : 0u);
         umma_commit(&bar.dk_done);
         umma_commit(&bar.q_empty[st]);
+        umma_commit(&bar.do_empty[t % KV_DOST]);   // D(t) is read until ds_ready(t)
       };
       mbar_wait(&bar.kv_full, 0, wc);
-      int t_sdp = 0, t_dv = 0, t_dk = 0;
-      uint64_t idle_since = 0;
-      while (t_dk < total && !bar.abort) {
-        bool progress = false;
-        if (t_sdp < total && (t_sdp == 0 || mbar_test(&bar.sdp_free, (t_sdp - 1) & 1)) &&
-            mbar_test(&bar.q_full[t_sdp & 1], (t_sdp >> 1) & 1) &&
-            mbar_test(&bar.do_full[t_sdp & 1], (t_sdp >> 1) & 1)) {
-          issue_sdp(t_sdp++);
-          progress = true;
-        }
-        if (t_dv < t_sdp && mbar_test(&bar.p_ready, t_dv & 1)) {
-          issue_dv(t_dv++);
-          progress = true;
-        }
-        if (t_dk < t_dv && mbar_test(&bar.ds_ready, t_dk & 1)) {
-          issue_dk(t_dk++);
-          progress = true;
-        }
-        if (progress) {
-          idle_since = 0;
-        } else if (idle_since == 0) {
-          idle_since = globaltimer_ns();
-        } else if (globaltimer_ns() - idle_since > a.timeout_ns) {
-          bar.abort = 1;
-          atomicOr(a.err, LCA_DEVERR_TIMEOUT);
+      if (total > 0) {
+        mbar_wait(&bar.q_full[0], 0, wc);
+        issue_s(0);
+        mbar_wait(&bar.do_full[0], 0, wc);
+        issue_dp(0);
+      }
+      for (int t = 0; t < total && !bar.abort; ++t) {
+        mbar_wait(&bar.p_ready, t & 1, wc);
+        issue_dv(t);
+        mbar_wait(&bar.ds_ready, t & 1, wc);
+        issue_dk(t);
+        const int n = t + 1;
+        if (n < total) {
+          mbar_wait(&bar.q_full[n % KV_QST], (n / KV_QST) & 1, wc);
+          mbar_wait(&bar.dv_done, t & 1, wc);      // P^T(t) consumed
+          issue_s(n);
+          mbar_wait(&bar.do_full[n % KV_DOST], (n / KV_DOST) & 1, wc);
+          mbar_wait(&bar.dk_done, t & 1, wc);      // dS^T(t) consumed
+          issue_dp(n);
         }
       }
     }
   } else {
+    // ------------------------------------------------ softmax warps 0-7
     const int quarter = warp & 3, half = warp >> 2;
-    const int row = quarter * 32 + lane;
+    const int jl = quarter * 32 + lane;              // key row within the tile = TMEM lane
+    const int j = kt * BN + jl;
+    const bool jvalid = j < S;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + half * 64;
-    const uint32_t spds = base_u32 + KV_OFF_PDS + half * HALF;
     const float sl2 = dm.scale_log2;
-    const int c0 = kt * BN + half * 64;
-    // LSE and D of the next pair are loaded one iteration ahead so their global-memory
-    // latency overlaps the current pair's work.
-    int h, qt, cls, t = 0;
-    bool have = walk.next(h, qt, cls);
-    float lse_next = 0.f, dsum_next = 0.f;
-    auto load_rows = [&](int hh, int qq) {
-      const int ii = qq * BM + row;
-      if (ii < S) {
-        const int64_t ri = (static_cast<int64_t>(b) * dm.h_q + hh) * S + ii;
-        lse_next = __ldg(a.lse + ri);
-        dsum_next = __ldg(a.dsum + ri);
-      }
-    };
-    if (have) load_rows(h, qt);
+    const RowSpan cs = col_span(a.mask, min(j, S - 1));
     MapCursor mcur;
-    while (have) {
-      const int i = qt * BM + row;
-      const bool valid = i < S;
-      const float lse2 = (!valid || lse_next == -INFINITY) ? INFINITY : lse_next * LOG2E;
-      const float dsum = valid ? dsum_next : 0.f;
+    int h, qt, cls, t = 0;
+    while (walk.next(h, qt, cls)) {
       const bool masked = cls != LCA_TILE_FULL || kt * BN + BN > S || qt * BM + BM > S;
       uint32_t bits[2] = {0u, 0u};
-      if (masked && valid) {
-        const RowSpan sp = row_span(a.mask, i);
-        row_tile_bits<2>(a.mask, h / dm.heads_per_map, i, c0, sp, bits, &mcur);
-      }
-      int h_n, qt_n, cls_n;
-      const bool have_n = walk.next(h_n, qt_n, cls_n);
-      if (have_n) load_rows(h_n, qt_n);
-      mbar_wait(&bar.sdp_full, t & 1, wc);
+      if (masked && jvalid)
+        col_tile_bits<2>(a.mask, h / dm.heads_per_map, j, qt * BM + half * 64, cs, bits, &mcur);
+      const float* lse2 =
+          reinterpret_cast<const float*>(base + KV_OFF_LSE + (t % KV_QST) * ROWV) + half * 64;
+      const float* dsum =
+          reinterpret_cast<const float*>(base + KV_OFF_D + (t % KV_DOST) * ROWV) + half * 64;
+
+      // The LSE2 / D rows were written by bulk copies that complete on q_full / do_full;
+      // observing those phases here (already complete: the stages are refilled only
+      // after this step's ds_ready) makes the rows visible to this thread.
+      mbar_wait(&bar.s_full, t & 1, wc);
+      mbar_wait(&bar.q_full[t % KV_QST], (t / KV_QST) & 1, wc);
       __syncwarp();
       tc_fence_after();
-      uint32_t sr[64], dr[64];
-      tmem_ld64x2(lane_addr + KV_TM_S, lane_addr + KV_TM_DP, sr, dr);
+      uint32_t r[64];
+      tmem_ld64(lane_addr + KV_TM_S, r);
+      float p[64];
+#pragma unroll
+      for (int x = 0; x < 64; x += 4) {
+        const float4 l = *reinterpret_cast<const float4*>(lse2 + x);
+        p[x + 0] = ex2_approx(fmaf(__uint_as_float(r[x + 0]), sl2, -l.x));
+        p[x + 1] = ex2_approx(fmaf(__uint_as_float(r[x + 1]), sl2, -l.y));
+        p[x + 2] = ex2_approx(fmaf(__uint_as_float(r[x + 2]), sl2, -l.z));
+        p[x + 3] = ex2_approx(fmaf(__uint_as_float(r[x + 3]), sl2, -l.w));
+      }
+      if (masked) {
+#pragma unroll
+        for (int x = 0; x < 64; ++x)
+          if (!((bits[x >> 5] >> (x & 31)) & 1u)) p[x] = 0.f;
+      }
+      uint32_t pk[32];
+#pragma unroll
+      for (int x = 0; x < 32; ++x) pk[x] = pack_bf16x2(p[2 * x], p[2 * x + 1]);
+      tmem_st32(lane_addr + KV_TM_S, pk);
       tc_fence_before();
-      mbar_arrive(&bar.sdp_free);
-      uint32_t pk[32], dk[32];
-      p_ds_half<true>(sr, dr, masked, bits, sl2, lse2, dsum, pk, dk);
-      if (t >= 1) mbar_wait(&bar.dk_done, (t - 1) & 1, wc);
-      __syncwarp();
-      store_half_row(spds, row, pk);
-      fence_proxy_async_smem();
       mbar_arrive(&bar.p_ready);
-      mbar_wait(&bar.dv_done, t & 1, wc);
+
+      mbar_wait(&bar.dp_full, t & 1, wc);
+      mbar_wait(&bar.do_full[t % KV_DOST], (t / KV_DOST) & 1, wc);
       __syncwarp();
-      store_half_row(spds, row, dk);
-      fence_proxy_async_smem();
+      tc_fence_after();
+      tmem_ld64(lane_addr + KV_TM_DP, r);
+#pragma unroll
+      for (int x = 0; x < 64; x += 4) {
+        const float4 dd = *reinterpret_cast<const float4*>(dsum + x);
+        p[x + 0] *= __uint_as_float(r[x + 0]) - dd.x;
+        p[x + 1] *= __uint_as_float(r[x + 1]) - dd.y;
+        p[x + 2] *= __uint_as_float(r[x + 2]) - dd.z;
+        p[x + 3] *= __uint_as_float(r[x + 3]) - dd.w;
+      }
+#pragma unroll
+      for (int x = 0; x < 32; ++x) pk[x] = pack_bf16x2(p[2 * x], p[2 * x + 1]);
+      tmem_st32(lane_addr + KV_TM_DP, pk);
+      tc_fence_before();
       mbar_arrive(&bar.ds_ready);
       ++t;
-      have = have_n;
-      h = h_n;
-      qt = qt_n;
-      cls = cls_n;
     }
     if (t > 0) {
+      mbar_wait(&bar.dv_done, (t - 1) & 1, wc);
       mbar_wait(&bar.dk_done, (t - 1) & 1, wc);
       __syncwarp();
       tc_fence_after();
     }
-    const int j = kt * BN + row;
-    const bool write = j < S;
     const int64_t roff = (static_cast<int64_t>(b) * S + j) * a.k_row_stride +
                          static_cast<int64_t>(hk) * HD + half * 64;
-    store_acc_half(lane_addr + KV_TM_DV, t > 0, 1.f, a.dv + roff, write);
-    store_acc_half(lane_addr + KV_TM_DK, t > 0, dm.scale, a.dk + roff, write);
+    store_acc_half(lane_addr + KV_TM_DV, t > 0, 1.f, a.dv + roff, jvalid);
+    store_acc_half(lane_addr + KV_TM_DK, t > 0, dm.scale, a.dk + roff, jvalid);
   }
 
   tc_fence_before();
@@ -676,13 +712,10 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     const uint32_t quarter_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const uint32_t lane_addr = quarter_addr + half * 64;
     const float sl2 = dm.scale_log2;
-    const int64_t rowi = (static_cast<int64_t>(b) * dm.h_q + h) * S + i;
-    float lse2 = INFINITY, dsum = 0.f;
-    if (valid) {
-      const float l = __ldg(a.lse + rowi);
-      lse2 = (l == -INFINITY) ? INFINITY : l * LOG2E;
-      dsum = __ldg(a.dsum + rowi);
-    }
+    // padded workspace rows: +inf / 0 on rows without keys and past S
+    const int64_t rowi = (static_cast<int64_t>(b) * dm.h_q + h) * a.s_pad + i;
+    const float lse2 = __ldg(a.lse2 + rowi);
+    const float dsum = __ldg(a.dsum + rowi);
     const RowSpan sp = row_span(a.mask, min(i, S - 1));
     MapCursor mcur;
     for (int n = 0; n < n_tiles; ++n) {
@@ -728,7 +761,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 }  // namespace
 
 cudaError_t launch_bwd_preprocess(const BwdArgs& a, cudaStream_t st) {
-  const int64_t rows = static_cast<int64_t>(a.dims.batch) * a.dims.seqlen * a.dims.h_q;
+  const int64_t rows = static_cast<int64_t>(a.dims.batch) * a.s_pad * a.dims.h_q;
   const int64_t blocks = (rows * 16 + 255) / 256;
   bwd_preprocess_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(a);
   return cudaGetLastError();

@@ -1,12 +1,12 @@
 // lca_attn_bwd_noalloc: the backward pass for callers that cannot allocate device
 // memory.
 //
-// lca_attn_bwd needs a caller-provided workspace (the per-row D = rowsum(dO * O)
-// buffer, fp32 [batch, h_q, seqlen]).  Some callers cannot call cudaMalloc at that
-// point: code running while a CUDA graph is being captured on their stream, custom
-// allocators that forbid side allocations, or runtimes that hand out only the
-// tensors of the op itself.  This entry point takes the workspace from a fixed
-// buffer compiled into the library instead, and otherwise runs exactly the
+// lca_attn_bwd needs a caller-provided workspace (per-row LSE*log2(e) and
+// D = rowsum(dO * O), fp32, rows padded to whole 128-row tiles).  Some callers cannot
+// call cudaMalloc at that point: code running while a CUDA graph is being captured on
+// their stream, custom allocators that forbid side allocations, or runtimes that hand
+// out only the tensors of the op itself.  This entry point takes the workspace from a
+// fixed buffer compiled into the library instead, and otherwise runs exactly the
 // lca_attn_bwd path.
 #include <cuda_runtime.h>
 
@@ -16,11 +16,12 @@
 
 namespace {
 
-// Capacity of the built-in workspace in rows of D (batch * h_q * seqlen), 32 MiB.
-constexpr size_t kMaxRows = size_t(1) << 23;
+// Capacity of the built-in workspace: two fp32 values for each of 2^23 padded rows
+// (batch * h_q * seqlen rounded up to 128), 64 MiB.
+constexpr size_t kScratchFloats = size_t(1) << 24;
 
 // The buffer lives in every GPU that loads the library, for the life of the process.
-static __device__ __align__(256) float g_bwd_scratch[kMaxRows];
+static __device__ __align__(256) float g_bwd_scratch[kScratchFloats];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
@@ -50,12 +51,11 @@ extern "C" lca_status lca_attn_bwd_noalloc(const lca_plan* plan, const lca_shape
                                            void* stream) {
   if (!plan || !shape) return LCA_ERR_INVALID_ARG;
   if (shape->batch < 1 || shape->h_q < 1 || shape->seqlen < 1) return LCA_ERR_INVALID_ARG;
-  const size_t rows = static_cast<size_t>(shape->batch) * static_cast<size_t>(shape->h_q) *
-                      static_cast<size_t>(shape->seqlen);
-  if (rows > kMaxRows) return LCA_ERR_UNSUPPORTED;
+  if (lca_attn_bwd_workspace(plan, shape, 0) > kScratchFloats * sizeof(float))
+    return LCA_ERR_UNSUPPORTED;
   float* scratch = nullptr;
   lca_status s = scratch_on_current_device(&scratch);
   if (s != LCA_OK) return s;
   return lca_attn_bwd(plan, shape, q, k, v, o, dout, lse, dq, dk, dv, scratch,
-                      kMaxRows * sizeof(float), softmax_scale, 0, stream);
+                      kScratchFloats * sizeof(float), softmax_scale, 0, stream);
 }

@@ -26,8 +26,11 @@ struct BwdArgs {
   MaskDev mask;
   const __nv_bfloat16* o;
   const __nv_bfloat16* dout;
-  const float* lse;
-  float* dsum;              // D = rowsum(dO * O), [B, H_q, S]
+  const float* lse;         // forward LSE, [B, H_q, S]
+  float* lse2;              // workspace: LSE * log2(e) (+inf for rows without keys and
+                            // padding), [B, H_q, s_pad]
+  float* dsum;              // workspace: D = rowsum(dO * O) (0 on padding), [B, H_q, s_pad]
+  int64_t s_pad;            // seqlen rounded up to the 128-row tile
   __nv_bfloat16* dq;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;

@@ -131,6 +131,16 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+// Untiled bulk copy of `bytes` from global to shared memory, completing on `bar` like
+// a tensor load (both addresses 16-byte aligned, `bytes` a multiple of 16).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // Prefetch a 4-D tile into L2 (no shared memory, no completion tracking): issued a few
 // steps ahead of the real load so that load hits in L2.
 __device__ __forceinline__ void tma_prefetch_l2_4d(const CUtensorMap* map, int c0, int c1, int c2,
@@ -450,6 +460,72 @@ __device__ __forceinline__ RowSpan row_span(const MaskDev& m, int i) {
   return r;
 }
 
+// Allowed queries of key column j as two disjoint half-open intervals inside [0, S):
+// the column view of row_span, for kernels whose threads own key rows.  Block-sparse
+// masks return their base interval (documents / causal), which the block map further
+// restricts.
+__device__ __forceinline__ RowSpan col_span(const MaskDev& m, int j) {
+  RowSpan r{0, 0, 0, 0};
+  const int S = m.seqlen;
+  const auto clip = [S](long long x) { return static_cast<int>(min(static_cast<long long>(S), x)); };
+  switch (m.type) {
+    case LCA_FULL: r.b0 = S; break;
+    case LCA_CAUSAL: r.a0 = j; r.b0 = S; break;
+    case LCA_SLIDING_WINDOW:  // j <= i < j + w
+      r.a0 = j; r.b0 = clip(static_cast<long long>(j) + m.window);
+      break;
+    case LCA_FULL_DOCUMENT: {
+      const int d = seg_find(m.cu, m.num_segments, j);
+      r.a0 = __ldg(m.cu + d); r.b0 = __ldg(m.cu + d + 1);
+    } break;
+    case LCA_CAUSAL_DOCUMENT: {
+      const int d = seg_find(m.cu, m.num_segments, j);
+      r.a0 = j; r.b0 = __ldg(m.cu + d + 1);
+    } break;
+    case LCA_PREFIX_LM:       // prefix keys are seen by every query
+      r.a0 = j < m.prefix_len ? 0 : j; r.b0 = S;
+      break;
+    case LCA_SHARED_QUESTION: {
+      const int s = seg_find(m.cu, m.num_segments, j);
+      r.a0 = j;               // question keys: every later query; answer keys: own answer
+      r.b0 = s == 0 ? S : __ldg(m.cu + s + 1);
+    } break;
+    case LCA_GLOBAL_SLIDING: {
+      if (m.base_causal) {
+        r.a0 = j;
+        r.b0 = j < m.num_global ? S : clip(static_cast<long long>(j) + m.window);
+      } else if (j < m.num_global) {
+        r.b0 = S;
+      } else {                // global queries, plus the symmetric window |i - j| < w
+        const int g = min(m.num_global, S);
+        const int wlo = max(0, j - m.window + 1);
+        const int whi = clip(static_cast<long long>(j) + m.window);
+        if (wlo <= g) { r.b0 = whi; }
+        else { r.b0 = g; r.a1 = wlo; r.b1 = whi; }
+      }
+    } break;
+    case LCA_CAUSAL_BLOCKWISE:
+      r.a0 = (j / m.block) * m.block; r.b0 = S;
+      break;
+    case LCA_BLOCK_CAUSAL_DOCUMENT: {
+      const int d = seg_find(m.cu, m.num_segments, j);
+      const int st = __ldg(m.cu + d);
+      r.a0 = st + ((j - st) / m.block) * m.block; r.b0 = __ldg(m.cu + d + 1);
+    } break;
+    default: {  // block-sparse base
+      int lo = 0, hi = S;
+      if (m.num_segments > 0) {
+        const int d = seg_find(m.cu, m.num_segments, j);
+        lo = __ldg(m.cu + d); hi = __ldg(m.cu + d + 1);
+      }
+      r.a0 = m.base_causal ? max(lo, j) : lo; r.b0 = hi;
+    } break;
+  }
+  if (r.b0 < r.a0) r.b0 = r.a0;
+  if (r.b1 < r.a1) r.b1 = r.a1;
+  return r;
+}
+
 __device__ __forceinline__ bool is_sparse(int type) {
   return type == LCA_BLOCK_SPARSE_UNIFORM || type == LCA_BLOCK_SPARSE_VARIABLE;
 }
@@ -507,6 +583,50 @@ __device__ __forceinline__ void row_tile_bits(const MaskDev& m, int h_m, int i, 
         const int hi = __ldg(co + cb + 1);
 #pragma unroll
         for (int w = 0; w < NW; ++w) mb[w] |= range_bits(lo, hi, c0 + 32 * w);
+      }
+    }
+  }
+#pragma unroll
+  for (int w = 0; w < NW; ++w) bits[w] &= mb[w];
+}
+
+// Allowed-query bits of key column j over the NW*32 queries starting at r0 (bit r of
+// word w = query r0 + 32w + r), from the column span `sp` and, for the sparse masks,
+// the block map's column of j.  Queries >= S are never allowed.
+template <int NW>
+__device__ __forceinline__ void col_tile_bits(const MaskDev& m, int h_m, int j, int r0,
+                                              const RowSpan& sp, uint32_t (&bits)[NW],
+                                              MapCursor* cur) {
+#pragma unroll
+  for (int w = 0; w < NW; ++w)
+    bits[w] = range_bits(sp.a0, sp.b0, r0 + 32 * w) | range_bits(sp.a1, sp.b1, r0 + 32 * w);
+  if (!is_sparse(m.type)) return;
+  uint32_t mb[NW];
+#pragma unroll
+  for (int w = 0; w < NW; ++w) mb[w] = 0u;
+  const int r1 = min(r0 + NW * 32, m.seqlen);
+  const uint8_t* map = m.bmap + static_cast<size_t>(h_m) * m.n_rb * m.n_cb;
+  if (m.type == LCA_BLOCK_SPARSE_UNIFORM) {
+    const int cb = j / m.block;
+    for (int rb = r0 / m.block; rb * m.block < r1; ++rb) {
+      if (__ldg(map + static_cast<size_t>(rb) * m.n_cb + cb)) {
+        const int lo = rb * m.block, hi = lo + m.block;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) mb[w] |= range_bits(lo, hi, r0 + 32 * w);
+      }
+    }
+  } else {
+    const int32_t* ro = m.row_off + static_cast<size_t>(h_m) * (m.n_rb + 1);
+    const int32_t* co = m.col_off + static_cast<size_t>(h_m) * (m.n_cb + 1);
+    const int cb = cur->cb = seg_find_from(co, m.n_cb, cur->cb, j);
+    const int rb0 = cur->rb = seg_find_from(ro, m.n_rb, cur->rb, r0);
+    for (int rb = rb0; rb < m.n_rb; ++rb) {
+      const int lo = __ldg(ro + rb);
+      if (lo >= r1) break;
+      if (__ldg(map + static_cast<size_t>(rb) * m.n_cb + cb)) {
+        const int hi = __ldg(ro + rb + 1);
+#pragma unroll
+        for (int w = 0; w < NW; ++w) mb[w] |= range_bits(lo, hi, r0 + 32 * w);
       }
     }
   }

@@ -37,7 +37,7 @@ def test_noalloc_backward_matches_allocating_backward_twice():
 
 def test_noalloc_backward_rejects_shapes_beyond_its_buffer():
     lib = binding.load_library()
-    s = 131073                      # 64 heads x 131073 rows > 2^23 rows of D
+    s = 131073                      # 64 heads x 131200 padded rows > 2^23
     plan = lca.mask_build(I.make_desc(I.FULL, s), 128, 128)
     sh = binding.ShapeC(1, s, 64, 8, 128, 64 * 128, 8 * 128, 8 * 128, 64 * 128)
     dummy = torch.empty(16, dtype=torch.bfloat16, device="cuda")
