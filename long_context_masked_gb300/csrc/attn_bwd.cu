@@ -6,20 +6,20 @@
 // mask and D = rowsum(dO * O):
 //   dV = P^T dO,  dP = dO V^T,  dS = P * (dP - D),  dK = scale dS^T Q,  dQ = scale dS K.
 // Three kernels, deterministic and free of floating-point atomics:
-//   preprocess  D for every (b, h, i) row (HBM-bound);
-//   dK/dV       one CTA per (KV head, key tile): loops over the query tiles that attend
-//               to the key tile (the plan's transposed lists) for every query head of
-//               the KV group, recomputing S and dP with tcgen05 and accumulating dV and
-//               dK in TMEM;
-//   dQ          one CTA per (query head, query tile): loops over the tile's key tiles,
-//               recomputing S, dP and dS and accumulating dQ in TMEM; dS goes to TMEM
-//               (bf16 pairs) and feeds the dQ MMA from there.
-// Warp roles as in the forward: warp 8 issues TMA loads, warp 9 owns TMEM and issues
-// the MMAs, warps 0-7 (two threads per query row, 64 key columns each) load their
-// halves of S and dP from TMEM behind one wait - which frees both accumulators at once,
-// so the next S/dP MMAs overlap the exp work - and turn them into P and dS (bf16,
-// 128-byte-swizzled shared tiles).  The same shared P/dS tile is read K-major (as dS
-// for dQ) or MN-major (as P^T / dS^T for dV / dK).  All waits are bounded.
+//   preprocess  D for every (b, h, i) row and LSE * log2(e), into padded workspace
+//               rows (HBM-bound);
+//   dK/dV       one CTA per (KV head, key tile), key rows on the TMEM lanes: loops over
+//               the query tiles that attend to the key tile (the plan's transposed
+//               lists) for every query head of the KV group, recomputing S^T and dP^T
+//               with tcgen05, writing P^T and dS^T back into TMEM and accumulating dV
+//               and dK there with TS MMAs;
+//   dQ          one CTA per (query head, query tile), query rows on the TMEM lanes:
+//               loops over the tile's key tiles, recomputing S, dP and dS and
+//               accumulating dQ in TMEM; dO and dS live in TMEM (bf16 pairs) and feed
+//               the dP and dQ MMAs from there.
+// Warp roles as in the forward: warps 8 and 10 issue TMA loads, warp 9 owns TMEM and
+// issues the MMAs, warps 0-7 (two threads per TMEM lane, 64 columns each) turn S/dP
+// into P/dS.  All waits are bounded.
 #include <cuda_runtime.h>
 
 #include "attn_kernels.h"
@@ -80,18 +80,16 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(BwdArgs a) {
 
 // ------------------------------------------------------------------ shared pieces
 
-constexpr int KV_THREADS = 352;      // dK/dV: 8 softmax warps, producer, MMA issuer, dO producer
+constexpr int KV_THREADS = 352;      // dK/dV: 8 softmax warps, Q producer, MMA issuer, dO producer
 constexpr int DQ_THREADS = 352;      // dQ: the same plus a second producer warp
 constexpr int SOFTMAX_THREADS = 256;
 constexpr int WARP_PRODUCER = 8, WARP_MMA = 9, WARP_PRODUCER_2 = 10;
 
-// Half a row (64 key columns) of P = exp2(s * scale_log2 - lse_log2) on allowed
-// entries and dS = P (dP - D), packed to bf16 pairs (P only when WANT_P).
-template <bool WANT_P>
-__device__ __forceinline__ void p_ds_half(const uint32_t (&sr)[64], const uint32_t (&dr)[64],
-                                          bool masked, const uint32_t (&bits)[2], float sl2,
-                                          float lse2, float dsum, uint32_t (&pk)[32],
-                                          uint32_t (&dk)[32]) {
+// Half a row (64 key columns) of dS = P (dP - D), P = exp2(s * scale_log2 - lse_log2)
+// on allowed entries, packed to bf16 pairs.
+__device__ __forceinline__ void ds_half(const uint32_t (&sr)[64], const uint32_t (&dr)[64],
+                                        bool masked, const uint32_t (&bits)[2], float sl2,
+                                        float lse2, float dsum, uint32_t (&dk)[32]) {
 #pragma unroll
   for (int x = 0; x < 64; x += 2) {
     float p0 = ex2_approx(fmaf(__uint_as_float(sr[x]), sl2, -lse2));
@@ -100,21 +98,9 @@ __device__ __forceinline__ void p_ds_half(const uint32_t (&sr)[64], const uint32
       if (!((bits[x >> 5] >> (x & 31)) & 1u)) p0 = 0.f;
       if (!((bits[x >> 5] >> ((x + 1) & 31)) & 1u)) p1 = 0.f;
     }
-    const float d0 = p0 * (__uint_as_float(dr[x]) - dsum);
-    const float d1 = p1 * (__uint_as_float(dr[x + 1]) - dsum);
-    if (WANT_P) pk[x / 2] = pack_bf16x2(p0, p1);
-    dk[x / 2] = pack_bf16x2(d0, d1);
+    dk[x / 2] = pack_bf16x2(p0 * (__uint_as_float(dr[x]) - dsum),
+                            p1 * (__uint_as_float(dr[x + 1]) - dsum));
   }
-}
-
-// Store half a row (64 packed bf16 pairs -> 64 columns) into one swizzled [128][64]
-// half of a [128][128] tile.
-__device__ __forceinline__ void store_half_row(uint32_t half_tile, int row,
-                                               const uint32_t (&v)[32]) {
-#pragma unroll
-  for (int u = 0; u < 8; ++u)
-    st_shared_v4(half_tile + sw128_offset(row, u), v[u * 4], v[u * 4 + 1], v[u * 4 + 2],
-                 v[u * 4 + 3]);
 }
 
 // Read 64 fp32 accumulator columns of this thread's lane, scale, store 64 bf16.
@@ -518,19 +504,21 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
 // ------------------------------------------------------------------ dQ
 
-constexpr int DQ_KST = 3;                        // K stages (K is held until the dQ MMA)
+// dO only ever feeds dP = dO V^T as the A operand, so it sits in TMEM (bf16 pairs, 64
+// columns, stored once per CTA by the softmax threads) and dP is a TS MMA; the shared
+// memory it frees gives K (held from S to dQ) a fourth stage.
+constexpr int DQ_KST = 4;                        // K stages (K is held until the dQ MMA)
 constexpr int DQ_VST = 2;                        // V stages (V is released after dP)
 constexpr uint32_t DQ_OFF_Q = 0;
-constexpr uint32_t DQ_OFF_DO = TILE;
-constexpr uint32_t DQ_OFF_K = 2 * TILE;
+constexpr uint32_t DQ_OFF_K = TILE;
 constexpr uint32_t DQ_OFF_V = DQ_OFF_K + DQ_KST * TILE;
 constexpr uint32_t DQ_OFF_BAR = DQ_OFF_V + DQ_VST * TILE;
 constexpr uint32_t DQ_SMEM = DQ_OFF_BAR + 256;    // the dynamic base is 1024-aligned
 static_assert(DQ_SMEM <= 232448, "dynamic shared memory above the 227 KB per-CTA limit");
-constexpr uint32_t DQ_TM_S = 0, DQ_TM_DP = 128, DQ_TM_DQ = 256, DQ_TM_DS = 384;
+constexpr uint32_t DQ_TM_S = 0, DQ_TM_DP = 128, DQ_TM_DQ = 256, DQ_TM_DS = 384, DQ_TM_DO = 448;
 
 struct DqBars {
-  uint64_t qdo_full;
+  uint64_t q_full, do_ready;
   uint64_t k_full[DQ_KST], k_empty[DQ_KST], v_full[DQ_VST], v_empty[DQ_VST];
   uint64_t sdp_full, sdp_free, ds_ready, dq_done;
   uint32_t tmem_base;
@@ -565,9 +553,11 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   const int hk = h / dm.group;
   const int beg = __ldg(pl.rowptr + row);
   const int n_tiles = __ldg(pl.rowptr + row + 1) - beg;
+  const auto tile = [&](int n) { return beg + n; };
 
   if (threadIdx.x == 0) {
-    mbar_init(&bar.qdo_full, 1);
+    mbar_init(&bar.q_full, 1);
+    mbar_init(&bar.do_ready, SOFTMAX_THREADS);
     for (int s = 0; s < DQ_KST; ++s) {
       mbar_init(&bar.k_full[s], 1);
       mbar_init(&bar.k_empty[s], 1);
@@ -595,16 +585,14 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 
   if (warp == WARP_PRODUCER) {
     if (lane == 0) {
-      mbar_arrive_expect_tx(&bar.qdo_full, 2 * TILE);
-      for (int c = 0; c < 2; ++c) {
-        tma_load_4d(base + DQ_OFF_Q + c * HALF, &tm_q, &bar.qdo_full, c * 64, h, qt * BM, b);
-        tma_load_4d(base + DQ_OFF_DO + c * HALF, &tm_do, &bar.qdo_full, c * 64, h, qt * BM, b);
-      }
+      mbar_arrive_expect_tx(&bar.q_full, TILE);
+      for (int c = 0; c < 2; ++c)
+        tma_load_4d(base + DQ_OFF_Q + c * HALF, &tm_q, &bar.q_full, c * 64, h, qt * BM, b);
       for (int n = 0; n < n_tiles; ++n) {
-        const int kt = __ldg(pl.kt_idx + beg + n);
+        const int kt = __ldg(pl.kt_idx + tile(n));
         const int st = n % DQ_KST;
         if (n + DQ_KST < n_tiles) {
-          const int ka = __ldg(pl.kt_idx + beg + n + DQ_KST);
+          const int ka = __ldg(pl.kt_idx + tile(n + DQ_KST));
           for (int c = 0; c < 2; ++c) tma_prefetch_l2_4d(&tm_k, c * 64, hk, ka * BN, b);
         }
         if (n >= DQ_KST) mbar_wait(&bar.k_empty[st], (n / DQ_KST - 1) & 1, wc);
@@ -614,7 +602,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                       kt * BN, b);
       }
       if (bar.abort) {
-        mbar_wait_final(&bar.qdo_full, 0, a.timeout_ns);
+        mbar_wait_final(&bar.q_full, 0, a.timeout_ns);
         for (int n = max(0, n_tiles - DQ_KST); n < n_tiles; ++n)
           mbar_wait_final(&bar.k_full[n % DQ_KST], (n / DQ_KST) & 1, a.timeout_ns);
       }
@@ -624,10 +612,10 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       // V stages are released after dP, earlier than K stages (released after dQ):
       // a separate warp keeps V loads from queueing behind K releases
       for (int n = 0; n < n_tiles; ++n) {
-        const int kt = __ldg(pl.kt_idx + beg + n);
+        const int kt = __ldg(pl.kt_idx + tile(n));
         const int st = n % DQ_VST;
         if (n + DQ_VST < n_tiles) {
-          const int ka = __ldg(pl.kt_idx + beg + n + DQ_VST);
+          const int ka = __ldg(pl.kt_idx + tile(n + DQ_VST));
           for (int c = 0; c < 2; ++c) tma_prefetch_l2_4d(&tm_v, c * 64, hk, ka * BN, b);
         }
         if (n >= DQ_VST) mbar_wait(&bar.v_empty[st], (n / DQ_VST - 1) & 1, wc);
@@ -646,7 +634,6 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       constexpr uint32_t IDESC_NT = idesc_bf16(BM, BN, 0, 0);  // S, dP
       constexpr uint32_t IDESC_NN = idesc_bf16(BM, HD, 0, 1);  // dQ (B = K MN-major)
       const uint64_t dq_ = desc_kmajor(base_u32 + DQ_OFF_Q, 0, HALF);
-      const uint64_t ddo_ = desc_kmajor(base_u32 + DQ_OFF_DO, 0, HALF);
       const uint64_t dk_k0 = desc_kmajor(base_u32 + DQ_OFF_K, 0, HALF);
       const uint64_t dk_m0 = desc_mnmajor(base_u32 + DQ_OFF_K, 0, HALF);
       const uint64_t dv_k0 = desc_kmajor(base_u32 + DQ_OFF_V, 0, HALF);
@@ -654,20 +641,22 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       // their inputs are ready so that a late K/V tile for SdP(n+1) never holds back
       // dQ(n).  SdP(n+1) needs the softmax's release of S/dP(n); the softmax writes
       // dS(n+1) only after dQ(n) completed, so ds_ready is at most one phase ahead.
+      // dP first: its commit releases the V stage half a group earlier, and S (the last
+      // reader of K until dQ) gets its K tile later.
       auto issue_sdp = [&](int n) {
         const uint64_t dk = dk_k0 + (n % DQ_KST) * stage_step(TILE);
         const uint64_t dv = dv_k0 + (n % DQ_VST) * stage_step(TILE);
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk)
-          umma_bf16_ss(tmem + DQ_TM_S, dq_ + kmajor_step(kk, HALF), dk + kmajor_step(kk, HALF),
+          umma_bf16_ts(tmem + DQ_TM_DP, tmem + DQ_TM_DO + kk * 8, dv + kmajor_step(kk, HALF),
                        IDESC_NT, kk > 0 ? 1u : 0u);
+        umma_commit(&bar.v_empty[n % DQ_VST]);
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk)
-          umma_bf16_ss(tmem + DQ_TM_DP, ddo_ + kmajor_step(kk, HALF), dv + kmajor_step(kk, HALF),
+          umma_bf16_ss(tmem + DQ_TM_S, dq_ + kmajor_step(kk, HALF), dk + kmajor_step(kk, HALF),
                        IDESC_NT, kk > 0 ? 1u : 0u);
         umma_commit(&bar.sdp_full);
-        umma_commit(&bar.v_empty[n % DQ_VST]);
       };
       auto issue_dq = [&](int n) {
         const uint64_t dk = dk_m0 + (n % DQ_KST) * stage_step(TILE);
@@ -679,7 +668,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         umma_commit(&bar.dq_done);
         umma_commit(&bar.k_empty[n % DQ_KST]);
       };
-      mbar_wait(&bar.qdo_full, 0, wc);
+      mbar_wait(&bar.q_full, 0, wc);
+      mbar_wait(&bar.do_ready, 0, wc);
       int n_sdp = 0, n_dq = 0;
       uint64_t idle_since = 0;
       while (n_dq < n_tiles && !bar.abort) {
@@ -716,11 +706,31 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     const int64_t rowi = (static_cast<int64_t>(b) * dm.h_q + h) * a.s_pad + i;
     const float lse2 = __ldg(a.lse2 + rowi);
     const float dsum = __ldg(a.dsum + rowi);
+    const int64_t roff = (static_cast<int64_t>(b) * S + i) * a.o_row_stride +
+                         static_cast<int64_t>(h) * HD + half * 64;
+    {
+      // this thread's half row of dO (64 bf16) into TMEM columns [DQ_TM_DO + 32 half, +32)
+      uint32_t v[32];
+      if (valid) {
+        const uint4* src = reinterpret_cast<const uint4*>(a.dout + roff);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint4 w = __ldg(src + u);
+          v[4 * u] = w.x; v[4 * u + 1] = w.y; v[4 * u + 2] = w.z; v[4 * u + 3] = w.w;
+        }
+      } else {
+#pragma unroll
+        for (int u = 0; u < 32; ++u) v[u] = 0u;
+      }
+      tmem_st32(quarter_addr + DQ_TM_DO + half * 32, v);
+      tc_fence_before();
+      mbar_arrive(&bar.do_ready);
+    }
     const RowSpan sp = row_span(a.mask, min(i, S - 1));
     MapCursor mcur;
     for (int n = 0; n < n_tiles; ++n) {
-      const int kt = __ldg(pl.kt_idx + beg + n);
-      const int cls = __ldg(pl.kt_cls + beg + n);
+      const int kt = __ldg(pl.kt_idx + tile(n));
+      const int cls = __ldg(pl.kt_cls + tile(n));
       const bool masked = cls != LCA_TILE_FULL || kt * BN + BN > S || qt * BM + BM > S;
       uint32_t bits[2] = {0u, 0u};
       if (masked && valid) row_tile_bits<2>(a.mask, hm, i, kt * BN + half * 64, sp, bits, &mcur);
@@ -731,8 +741,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       tmem_ld64x2(lane_addr + DQ_TM_S, lane_addr + DQ_TM_DP, sr, dr);
       tc_fence_before();
       mbar_arrive(&bar.sdp_free);
-      uint32_t pk[32], dk[32];
-      p_ds_half<false>(sr, dr, masked, bits, sl2, lse2, dsum, pk, dk);
+      uint32_t dk[32];
+      ds_half(sr, dr, masked, bits, sl2, lse2, dsum, dk);
       if (n >= 1) mbar_wait(&bar.dq_done, (n - 1) & 1, wc);   // dQ_{n-1} read dS_{n-1}
       __syncwarp();
       tc_fence_after();
@@ -745,8 +755,6 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       __syncwarp();
       tc_fence_after();
     }
-    const int64_t roff = (static_cast<int64_t>(b) * S + i) * a.o_row_stride +
-                         static_cast<int64_t>(h) * HD + half * 64;
     store_acc_half(lane_addr + DQ_TM_DQ, n_tiles > 0, dm.scale, a.dq + roff, valid);
   }
 
