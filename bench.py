@@ -531,7 +531,7 @@ def run_gpu(args, rank, world):
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        v, secs, what = oracle_sample(groups, 256, seed=0, budget_s=30.0)
+        v, secs, what = oracle_sample(groups, 2048, seed=0, budget_s=30.0)
         cpu = {"value": v, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
                "sample": what + f" ({secs:.1f} s)"}
 
