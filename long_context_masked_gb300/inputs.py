@@ -200,6 +200,18 @@ def variable_block_map(seqlen: int, map_heads: int, seed: int, keep: float = 0.5
     return row_off, col_off, bmap
 
 
+def random_block_scores(map_heads: int, n_row_blocks: int, n_col_blocks: int,
+                        seed: int) -> np.ndarray:
+    """Random block importance scores, fp32 uniform in [0, 1), [H_m, n_rb, n_cb].
+
+    The benchmark scores blocks randomly so that only the block-sparse attention
+    itself is measured (appendix A.2, "Score Calculation"); a top-k selection over
+    these scores gives its top-k maps.
+    """
+    rng = np.random.Generator(np.random.PCG64(seed))
+    return rng.random((map_heads, n_row_blocks, n_col_blocks), dtype=np.float32)
+
+
 # ------------------------------------------------------------ descriptors
 
 def make_desc(mask_type: int, seqlen: int, *, window: int = 4096, num_global: int = 256,

@@ -91,3 +91,23 @@ def load_attention_closed_form():
             case, qty, idx, expr = ln.split(None, 3)
             out.append((case, qty, int(idx), float(eval(expr, {"math": math}))))
     return out
+
+
+def load_blockmap_cases():
+    """Sections of blockmap_small.txt as {name: {key: value text}}."""
+    out, cur = {}, None
+    with open(os.path.join(GOLDEN, "blockmap_small.txt")) as f:
+        for ln in f:
+            ln = ln.strip()
+            if not ln or ln.startswith("#"):
+                continue
+            if ln.startswith("["):
+                cur = out.setdefault(ln.strip("[]"), {})
+                continue
+            key, _, val = [x.strip() for x in ln.partition("=")]
+            cur[key] = val
+    return out
+
+
+def float_matrix(text):
+    return np.array([[float(x) for x in row.split(",")] for row in text.split(";")])
