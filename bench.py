@@ -52,7 +52,7 @@ FLUSH_BYTES = 256 << 20
 FWD_PER_PAIR, BWD_PER_PAIR = 4.0 * D, 10.0 * D
 KERNEL_SOURCES = {"attn_fwd": "attn_fwd.cu", "bwd_dkdv": "attn_bwd.cu", "bwd_dq": "attn_bwd.cu",
                   "bwd_preprocess": "attn_bwd.cu"}
-SUITES = ("dense", "heterogeneous", "sparse", "varlen")
+SUITES = ("dense", "heterogeneous", "sparse", "varlen", "dynamic")
 
 
 # ------------------------------------------------------------------ workloads
@@ -62,8 +62,12 @@ SUITES = ("dense", "heterogeneous", "sparse", "varlen")
 # descriptor and per_step says whether the descriptor is re-drawn every step.
 
 class Case:
-    def __init__(self, name, make, per_step=False):
+    def __init__(self, name, make, per_step=False, dynamic=None):
         self.name, self.make, self.per_step = name, make, per_step
+        # dynamic = (block, sparsity, map_heads): the block map is computed on the GPU
+        # inside the step (pooled block scores, then top-k); `make` then only gives the
+        # host descriptor the CPU oracle sample uses (a random-score top-k map)
+        self.dynamic = dynamic
 
 
 def dense_cases(s):
@@ -97,6 +101,19 @@ def sparse_cases(s, map_heads):
                                 I.BLOCK_SPARSE_UNIFORM, s, sparse_block=b, sparsity=sp,
                                 map_heads=map_heads, map_seed=1000 * b + int(10 * sp))))
     return out
+
+
+def dynamic_cases(s, map_heads, block=128, sparsity=0.5):
+    import oracle
+
+    nb = (s + block - 1) // block
+
+    def make(st):
+        k = oracle.topk_count(nb, sparsity)
+        bmap = oracle.topk_block_map(I.random_block_scores(1, nb, nb, seed=st), k)
+        return I.MaskDesc(I.BLOCK_SPARSE_UNIFORM, s, block=block, map_heads=1,
+                          n_row_blocks=nb, n_col_blocks=nb, block_map=bmap)
+    return [Case(f"POOLED_TOPK_b{block}_s{sparsity}", make, dynamic=(block, sparsity, map_heads))]
 
 
 def workload(suite, case=None):
@@ -135,6 +152,12 @@ def workload(suite, case=None):
                 "S=128K, GQA 64:8, d=128: CAUSAL_DOCUMENT (lognormal documents) AND one "
                 "variable block partition per KV head (block sizes 32..256, multiples of 16) "
                 "with 50% of the causal blocks kept")
+    if suite == "dynamic":
+        return ([(s, 64, 8, dynamic_cases(s, 8)) for s in (32768, 65536, 131072)],
+                "dynamic block-sparse masks: per step, block scores from mean-pooled Q/K "
+                "(128-blocks, one map per KV head), top-k per query block at sparsity 0.5, "
+                "plan build from the device map, then forward + backward; S in {32K, 64K, "
+                "128K}, GQA 64:8, d=128")
     raise ValueError(suite)
 
 
@@ -374,6 +397,8 @@ def run_gpu(args, rank, world):
     n_draws = min(DOC_RUNS, args.warmup + args.steps)
     for gi, (_, _, _, cases) in enumerate(groups):
         for ci, c in enumerate(cases):
+            if c.dynamic:
+                continue
             for st in (range(n_draws) if c.per_step else (0,)):
                 descs[(gi, ci, st)] = c.make(st)
 
@@ -393,7 +418,16 @@ def run_gpu(args, rank, world):
                 if timers is not None:
                     ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
                     ev[0].record(stream)
-                plan = lca.mask_build(desc_of(gi, ci, st), 128, 128)
+                if c.dynamic:
+                    blk, sparsity, hmaps = c.dynamic
+                    scores = lca.block_scores(q, k, blk, hmaps)
+                    nb = scores.shape[1]
+                    dmap = lca.block_topk(scores, max(1, min(nb, round((1 - sparsity) * nb))))
+                    desc = I.MaskDesc(I.BLOCK_SPARSE_UNIFORM, s, block=blk, map_heads=hmaps,
+                                      n_row_blocks=nb, n_col_blocks=nb, block_map=dmap)
+                else:
+                    desc = desc_of(gi, ci, st)
+                plan = lca.mask_build(desc, 128, 128)
                 if ev is not None:
                     ev[1].record(stream)
                 lca.attn_fwd(plan, q, k, v, out=d["o"], lse=d["lse"])
@@ -546,7 +580,7 @@ def run_gpu(args, rank, world):
                 "pages' corpora are not available)",
         "config": {"workload": text, "suite": "case" if args.case else args.suite,
                    "head_dim": D, "batch_per_gpu": 1, "tiles": "128x128",
-                   "step": "per (S, mask): mask build + forward + backward",
+                   "step": "per (S, mask): mask build (for dynamic masks: block scores + top-k + plan) + forward + backward",
                    "l2": "flushed before every timed step (256 MB write)",
                    "parallelism": f"replicas x{world} (independent batch entries, no collective)"},
         "headline": {

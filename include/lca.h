@@ -169,6 +169,42 @@ lca_status lca_attn_fwd(const lca_plan* plan, const lca_shape* shape, const void
                         const void* k, const void* v, void* o, float* lse, float softmax_scale,
                         void* stream);
 
+/* ---- block maps from block scores (dynamic block-sparse masks)
+ *
+ * The benchmark builds a sparse mask by scoring every (query block, key block) pair
+ * and keeping, for each query block, the k best key blocks, k following from the
+ * sparsity ratio ("Long-Context Attention Benchmark", appendix A.2: Score Calculation,
+ * Top-k Selection).  Its dynamic masks score blocks from the data, e.g. from
+ * mean-pooled queries and keys (appendix A.3, "VSA").  lca_block_scores computes such
+ * scores and lca_block_topk turns any score array into a block map that a
+ * LCA_BLOCK_SPARSE_UNIFORM descriptor can pass to lca_mask_build (as a device array). */
+
+/* Bytes of device workspace lca_block_scores needs: the pooled query and key blocks,
+ * 2 * map_heads * ceil(seqlen / block) * 128 fp32 (0 for invalid arguments). */
+size_t lca_block_scores_workspace(const lca_shape* shape, int block, int map_heads);
+
+/* scores[h_m][r][c] = scale * < mean of Q over the rows of query block r (rows clipped
+ * at seqlen) and the query heads of map head h_m,
+ *                              mean of K over the rows of key block c and the KV heads
+ * of those query heads >.
+ * Preconditions: batch 1, head_dim 128, h_q % h_kv == 0, 1 <= block <= seqlen,
+ * map_heads 1, h_kv or h_q (query heads h_m*h_q/map_heads .. +h_q/map_heads share a map
+ * head), row strides multiples of 8 elements, q/k/scores/workspace 16-byte aligned
+ * device pointers.  `scores` is a caller-owned device array of map_heads * n_b * n_b
+ * fp32 (n_b = ceil(seqlen / block)); `workspace` holds at least
+ * lca_block_scores_workspace() bytes.  softmax_scale <= 0 means 1/sqrt(128).
+ * Asynchronous on `stream`; invalid arguments return before any launch. */
+lca_status lca_block_scores(const lca_shape* shape, const void* q, const void* k, int block,
+                            int map_heads, float softmax_scale, float* scores, void* workspace,
+                            size_t ws_bytes, void* stream);
+
+/* Top-k selection per row: block_map[h][r][c] = 1 for the k largest scores[h][r][.]
+ * (descending score, ties by ascending c), 0 elsewhere.  scores: fp32 device array
+ * [map_heads][n_rows][n_cols] without NaNs; block_map: uint8 device array of the same
+ * shape (caller-owned).  Requires 1 <= k <= n_cols.  Asynchronous on `stream`. */
+lca_status lca_block_topk(const float* scores, int map_heads, int n_rows, int n_cols, int k,
+                          uint8_t* block_map, void* stream);
+
 /* Bytes of device workspace lca_attn_bwd needs: two fp32 rows per (batch, query head),
  * LSE * log2(e) and D = rowsum(dO * O), each padded to seqlen rounded up to 128, i.e.
  * 8 * batch * h_q * round_up(seqlen, 128) bytes (0 for a NULL plan or shape). */

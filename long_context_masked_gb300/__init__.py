@@ -7,7 +7,7 @@ package loads nothing: the binding and the library are loaded on first use.
 """
 _BINDING = ("Plan", "LcaError", "mask_build", "attn_fwd", "attn_bwd", "load_library",
             "library_path", "last_device_error", "selftest_umma", "selftest_wait_timeout",
-            "profile_enable", "profile_read", "attn_bwd_noalloc")
+            "profile_enable", "profile_read", "attn_bwd_noalloc", "block_scores", "block_topk")
 
 
 def __getattr__(name):

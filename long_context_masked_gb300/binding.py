@@ -90,6 +90,12 @@ def load_library():
         "lca_status_string": ([i32], ctypes.c_char_p),
         "lca_attn_bwd_noalloc": ([vp, ctypes.POINTER(ShapeC)] + [vp] * 9 + [f32, vp], i32),
         "lca_profile_enable": ([ctypes.c_int], None),
+        "lca_block_scores_workspace": ([ctypes.POINTER(ShapeC), ctypes.c_int, ctypes.c_int],
+                                       ctypes.c_size_t),
+        "lca_block_scores": ([ctypes.POINTER(ShapeC), vp, vp, ctypes.c_int, ctypes.c_int, f32, vp,
+                              vp, ctypes.c_size_t, vp], i32),
+        "lca_block_topk": ([vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp],
+                           i32),
         "lca_profile_read": ([ctypes.POINTER(KernelTimeC), ctypes.c_int], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
@@ -179,11 +185,20 @@ def mask_build(desc: I.MaskDesc, tile_q: int = 128, tile_k: int = 128, stream=No
         c.cu_seqlens = t.data_ptr()
     c.map_heads = desc.map_heads
     if desc.block_map is not None:
-        bm = np.asarray(desc.block_map, np.uint8)
-        t = _dev_array(bm, np.uint8, device)
+        bm = desc.block_map
+        if hasattr(bm, "data_ptr") and getattr(bm, "is_cuda", False):
+            # a device map (e.g. from block_topk) is passed as is
+            import torch
+
+            if bm.dtype != torch.uint8 or not bm.is_contiguous() or bm.dim() != 3:
+                raise LcaError("block_map: contiguous uint8 [map_heads, n_rb, n_cb] expected", 1)
+            t = bm
+        else:
+            bm = np.asarray(bm, np.uint8)
+            t = _dev_array(bm, np.uint8, device)
         keep.append(t)
         c.block_map = t.data_ptr()
-        c.n_row_blocks, c.n_col_blocks = bm.shape[1], bm.shape[2]
+        c.n_row_blocks, c.n_col_blocks = int(bm.shape[1]), int(bm.shape[2])
     for name in ("row_offsets", "col_offsets"):
         arr = getattr(desc, name)
         if arr is not None:
@@ -302,3 +317,42 @@ def profile_read() -> dict:
     if n < 0:
         raise LcaError("lca_profile_read", 3)
     return {buf[i].name.decode(): (int(buf[i].launches), float(buf[i].total_ms)) for i in range(n)}
+
+
+def block_scores(q, k, block: int, map_heads: int, scale: Optional[float] = None, out=None,
+                 workspace=None, stream=None):
+    """fp32 [map_heads, n_b, n_b] block scores from mean-pooled Q and K (lca_block_scores).
+    q [1, S, Hq, 128], k [1, S, Hkv, 128] bf16 on the GPU; n_b = ceil(S / block)."""
+    import torch
+
+    lib = load_library()
+    b, s, hq, d = q.shape
+    hkv = k.shape[2]
+    sh = ShapeC(b, s, hq, hkv, d, q.stride(1), k.stride(1), k.stride(1), q.stride(1))
+    nb = (s + block - 1) // block
+    scores = torch.empty((map_heads, nb, nb), dtype=torch.float32, device=q.device) \
+        if out is None else out
+    ws_bytes = lib.lca_block_scores_workspace(ctypes.byref(sh), block, map_heads)
+    if workspace is None:
+        workspace = torch.empty(max(1, ws_bytes // 4), dtype=torch.float32, device=q.device)
+    st = lib.lca_block_scores(ctypes.byref(sh), q.data_ptr(), k.data_ptr(), block, map_heads,
+                              float(scale) if scale else 0.0, scores.data_ptr(),
+                              workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                              _stream(stream))
+    _check("lca_block_scores", st)
+    return scores
+
+
+def block_topk(scores, k: int, out=None, stream=None):
+    """uint8 block map of the k best key blocks of every row of ``scores`` (lca_block_topk):
+    descending score, ties by ascending key block.  scores fp32 [H_m, n_rb, n_cb] on the GPU."""
+    import torch
+
+    lib = load_library()
+    if scores.dtype != torch.float32 or not scores.is_contiguous() or scores.dim() != 3:
+        raise LcaError("scores: contiguous fp32 [map_heads, n_rb, n_cb] expected", 1)
+    hm, nr, nc = scores.shape
+    m = torch.empty((hm, nr, nc), dtype=torch.uint8, device=scores.device) if out is None else out
+    st = lib.lca_block_topk(scores.data_ptr(), hm, nr, nc, int(k), m.data_ptr(), _stream(stream))
+    _check("lca_block_topk", st)
+    return m

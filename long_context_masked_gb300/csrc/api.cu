@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <climits>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -12,6 +13,7 @@
 #include <vector>
 
 #include "attn_kernels.h"
+#include "blockmap.h"
 #include "lca_types.h"
 #include "mask_build.h"
 #include "profile.h"
@@ -521,6 +523,60 @@ lca_status lca_attn_bwd(const lca_plan* plan, const lca_shape* shape, const void
     if (launch_bwd_dq(tq, tk, tv, tdo, a, n_q_blocks, st) != cudaSuccess) return LCA_ERR_CUDA;
   }
   return LCA_OK;
+}
+
+size_t lca_block_scores_workspace(const lca_shape* shape, int block, int map_heads) {
+  if (!shape || block < 1 || shape->seqlen < 1 || map_heads < 1) return 0;
+  const int n_b = (shape->seqlen + block - 1) / block;
+  return block_scores_workspace_bytes(map_heads, n_b);
+}
+
+lca_status lca_block_scores(const lca_shape* shape, const void* q, const void* k, int block,
+                            int map_heads, float softmax_scale, float* scores, void* workspace,
+                            size_t ws_bytes, void* stream) {
+  if (!shape || !q || !k || !scores || !workspace) return LCA_ERR_INVALID_ARG;
+  if (shape->batch != 1 || shape->head_dim != 128 || shape->seqlen < 1 || shape->h_q < 1 ||
+      shape->h_kv < 1 || shape->h_q % shape->h_kv != 0)
+    return LCA_ERR_INVALID_ARG;
+  if (block < 1 || block > shape->seqlen) return LCA_ERR_INVALID_ARG;
+  if (map_heads != 1 && map_heads != shape->h_kv && map_heads != shape->h_q)
+    return LCA_ERR_INVALID_ARG;
+  if (shape->q_row_stride < shape->h_q * 128 || shape->k_row_stride < shape->h_kv * 128 ||
+      shape->q_row_stride % 8 != 0 || shape->k_row_stride % 8 != 0)
+    return LCA_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k, scores, workspace};
+  for (const void* ptr : ptrs)
+    if (!aligned16(ptr)) return LCA_ERR_INVALID_ARG;
+  if (ws_bytes < lca_block_scores_workspace(shape, block, map_heads)) return LCA_ERR_INVALID_ARG;
+  BlockScoreArgs a;
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.k = static_cast<const __nv_bfloat16*>(k);
+  a.q_row_stride = shape->q_row_stride;
+  a.k_row_stride = shape->k_row_stride;
+  a.seqlen = shape->seqlen;
+  a.block = block;
+  a.n_blocks = (shape->seqlen + block - 1) / block;
+  a.map_heads = map_heads;
+  a.heads_per_map = shape->h_q / map_heads;
+  a.group = shape->h_q / shape->h_kv;
+  a.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(128.0f);
+  a.pooled = static_cast<float*>(workspace);
+  a.scores = scores;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  ProfScope ps(K_BLOCK_SCORES, st);
+  return launch_block_scores(a, st) == cudaSuccess ? LCA_OK : LCA_ERR_CUDA;
+}
+
+lca_status lca_block_topk(const float* scores, int map_heads, int n_rows, int n_cols, int k,
+                          uint8_t* block_map, void* stream) {
+  if (!scores || !block_map || map_heads < 1 || n_rows < 1 || n_cols < 1) return LCA_ERR_INVALID_ARG;
+  if (k < 1 || k > n_cols) return LCA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(map_heads) * n_rows > INT32_MAX) return LCA_ERR_UNSUPPORTED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  ProfScope ps(K_BLOCK_TOPK, st);
+  return launch_block_topk(scores, map_heads * n_rows, n_cols, k, block_map, st) == cudaSuccess
+             ? LCA_OK
+             : LCA_ERR_CUDA;
 }
 
 lca_status lca_get_last_device_error(void* stream) {

@@ -14,7 +14,8 @@ namespace lca {
 namespace {
 
 const char* kNames[K_COUNT] = {"mask_classify", "mask_scan", "mask_collen", "mask_fill",
-                               "mask_lpt", "attn_fwd", "bwd_preprocess", "bwd_dkdv", "bwd_dq"};
+                               "mask_lpt", "attn_fwd", "bwd_preprocess", "bwd_dkdv", "bwd_dq",
+                               "block_scores", "block_topk"};
 
 struct Rec {
   int id, launches;

@@ -84,3 +84,24 @@ def test_null_arguments(lib):
     info = binding.PlanInfoC()
     assert lib.lca_plan_get_info(None, ctypes.byref(info)) == 1
     lib.lca_plan_destroy(None)
+
+
+def test_block_map_entry_points_validate_before_launch(lib):
+    """Invalid shapes, sizes and pointers are rejected on the host (no GPU needed)."""
+    sh = binding.ShapeC(1, 1000, 8, 2, 128, 8 * 128, 2 * 128, 2 * 128, 8 * 128)
+    assert lib.lca_block_scores_workspace(ctypes.byref(sh), 64, 2) == 2 * 2 * 16 * 128 * 4
+    assert lib.lca_block_scores_workspace(ctypes.byref(sh), 0, 2) == 0
+    p, ws = 256, 1 << 20
+    ok = (ctypes.byref(sh), p, p, 64, 2, 0.0, p, p, ws, None)
+    for i, bad in [(3, 0), (3, 1001), (4, 3), (6, 0), (7, 0), (8, 16)]:
+        args = list(ok)
+        args[i] = bad
+        assert lib.lca_block_scores(*args) == 1, (i, bad)
+    sh2 = binding.ShapeC(2, 1000, 8, 2, 128, 8 * 128, 2 * 128, 2 * 128, 8 * 128)   # batch 2
+    assert lib.lca_block_scores(ctypes.byref(sh2), *ok[1:]) == 1
+    sh3 = binding.ShapeC(1, 1000, 8, 2, 64, 8 * 64, 2 * 64, 2 * 64, 8 * 64)        # head_dim 64
+    assert lib.lca_block_scores(ctypes.byref(sh3), *ok[1:]) == 1
+    assert lib.lca_block_topk(p, 2, 3, 10, 0, p, None) == 1
+    assert lib.lca_block_topk(p, 2, 3, 10, 11, p, None) == 1
+    assert lib.lca_block_topk(None, 2, 3, 10, 4, p, None) == 1
+    assert lib.lca_block_topk(p, 0, 3, 10, 4, p, None) == 1
