@@ -350,6 +350,20 @@ def tflops(flops, ms):
     return flops / (ms * 1e-3) / 1e12
 
 
+def memory_row(d, info, s, hq):
+    """Device memory of one (S, mask) case: the attention tensors this path holds (Q, K,
+    V, O, dO, dQ, dK, dV, LSE and the backward workspace, from the allocated tensors),
+    the plan (as the library reports it), and the activation memory of a standard
+    attention module by the pages' model 11bshd + 5bhs^2 + 2bshd, read as bytes with
+    hidden size h*d (LongCA-bench summary, appendix A.4.2)."""
+    tensors = sum(t.numel() * t.element_size()
+                  for t in list(d["dev"]) + [d[x] for x in ("o", "lse", "dq", "dk", "dv", "ws")])
+    model = (13 * s * hq * D + 5 * hq * s * s)
+    return {"attention_tensors_gb": round(tensors / 1e9, 3),
+            "plan_mb": round(info.get("device_bytes", 0) / 1e6, 2),
+            "standard_attention_model_gb": round(model / 1e9, 2)}
+
+
 def case_label(suite, s, hq, hkv, name):
     return f"S={s}/{name}" if suite == "dense" else f"S={s}/{hq}:{hkv}/{name}"
 
@@ -498,7 +512,7 @@ def run_gpu(args, rank, world):
         w_ms = ev[2].elapsed_time(ev[3])
         acc = per_cfg.setdefault(case_label(args.suite, s, hq, hkv, name),
                                  {"fwd": [], "bwd": [], "build_ms": [], "fwd_ms": [],
-                                  "bwd_ms": [], "info": info, "hq": hq})
+                                  "bwd_ms": [], "info": info, "hq": hq, "gi": gi, "s": s})
         acc["fwd"].append(tflops(FWD_PER_PAIR * hp, f_ms))
         acc["bwd"].append(tflops(BWD_PER_PAIR * hp, w_ms))
         acc["build_ms"].append(b_ms)
@@ -510,7 +524,8 @@ def run_gpu(args, rank, world):
         row = {"fwd_tflops": round(fwd, 1), "bwd_tflops": round(bwd, 1),
                "fwd_pct_peak": round(100 * fwd / pk["bf16"], 1),
                "bwd_pct_peak": round(100 * bwd / pk["bf16"], 1),
-               "build_ms": round(statistics.median(v["build_ms"]), 3)}
+               "build_ms": round(statistics.median(v["build_ms"]), 3),
+               "memory": memory_row(data[v["gi"]], v["info"], v["s"], v["hq"])}
         if not default:
             inf = v["info"]
             head_tiles = inf["nnz"] * (v["hq"] // inf["map_heads"])

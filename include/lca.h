@@ -130,11 +130,13 @@ typedef struct {
 
 typedef struct lca_plan lca_plan; /* opaque; owns its device buffers */
 
-/* Sizes of a plan's arrays, for lca_plan_export. */
+/* Sizes of a plan's arrays, for lca_plan_export, and its device footprint. */
 typedef struct {
   int32_t seqlen, tile_q, tile_k, n_qt, n_kt, map_heads, mask_type;
   int64_t nnz;         /* non-skipped tiles over all map heads                  */
   int64_t n_partial;   /* of which PARTIAL                                      */
+  int64_t device_bytes;  /* device memory the plan holds (its arrays and the copies
+                            of the descriptor's arrays)                          */
 } lca_plan_info;
 
 /* Build the tile plan of a mask (step "mask build": classify every (query tile, key

@@ -48,7 +48,7 @@ class PlanInfoC(ctypes.Structure):
     _fields_ = [("seqlen", ctypes.c_int32), ("tile_q", ctypes.c_int32), ("tile_k", ctypes.c_int32),
                 ("n_qt", ctypes.c_int32), ("n_kt", ctypes.c_int32), ("map_heads", ctypes.c_int32),
                 ("mask_type", ctypes.c_int32), ("nnz", ctypes.c_int64),
-                ("n_partial", ctypes.c_int64)]
+                ("n_partial", ctypes.c_int64), ("device_bytes", ctypes.c_int64)]
 
 
 class KernelTimeC(ctypes.Structure):

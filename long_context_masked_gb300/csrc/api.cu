@@ -161,6 +161,7 @@ struct lca_plan {
   PlanDev dev{};
   unsigned long long* n_valid = nullptr;
   std::vector<void*> allocs;
+  size_t bytes = 0;   // device memory held by the plan
 
   ~lca_plan() {
     for (void* p : allocs) cudaFree(p);
@@ -170,6 +171,7 @@ struct lca_plan {
     void* p = nullptr;
     if (cudaMalloc(&p, (n ? n : 1) * sizeof(T)) != cudaSuccess) return nullptr;
     allocs.push_back(p);
+    bytes += (n ? n : 1) * sizeof(T);
     return static_cast<T*>(p);
   }
 };
@@ -349,6 +351,7 @@ lca_status lca_mask_build(const lca_mask_desc* desc, int tile_q, int tile_k, voi
 lca_status lca_plan_get_info(const lca_plan* plan, lca_plan_info* info) {
   if (!plan || !info) return LCA_ERR_INVALID_ARG;
   *info = plan->info;
+  info->device_bytes = static_cast<int64_t>(plan->bytes);
   return LCA_OK;
 }
 

@@ -128,3 +128,18 @@ def test_plan_full_size_variable_sparse():
     g2 = lca.mask_build(small, 128, 128).export()
     for hm in range(2):
         assert g2["n_valid"][hm] == oracle.n_valid_popcount(small, hm)
+
+
+def test_plan_reports_its_device_memory():
+    """lca_plan_info.device_bytes covers at least the arrays lca_plan_export copies out
+    and the plan's copy of the block map."""
+    s = 2000
+    desc = I.make_desc(I.BLOCK_SPARSE_UNIFORM, s, sparse_block=64, sparsity=0.5, map_heads=2,
+                       map_seed=1)
+    plan = lca.mask_build(desc, 128, 128)
+    inf = plan.info
+    hm, nq, nk, nnz = inf["map_heads"], inf["n_qt"], inf["n_kt"], inf["nnz"]
+    exported = (hm * nq * nk + 4 * (hm * nq + 1) + 5 * nnz + 4 * (hm * nk + 1) + 5 * nnz
+                + 4 * hm * (nq + nk) + 8 * hm)
+    assert inf["device_bytes"] >= exported + desc.block_map.nbytes
+    assert inf["device_bytes"] < 4 * (exported + desc.block_map.nbytes) + (1 << 20)
