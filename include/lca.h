@@ -56,6 +56,7 @@ typedef enum {
  *   SLIDING_WINDOW         j <= i && i - j < window
  *   FULL_DOCUMENT          doc(i) == doc(j)                      (docs from cu_seqlens)
  *   CAUSAL_DOCUMENT        doc(i) == doc(j) && j <= i
+ *   SLIDING_WINDOW_DOCUMENT doc(i) == doc(j) && j <= i && i - j < window
  *   PREFIX_LM              j < prefix_len || j <= i
  *   SHARED_QUESTION        j <= i && (seg(j) == seg(i) || seg(j) == 0)  (segment 0 = question)
  *   GLOBAL_SLIDING         base_causal: j <= i && (j < num_global || i - j < window)
@@ -79,7 +80,8 @@ typedef enum {
   LCA_CAUSAL_BLOCKWISE = 8,
   LCA_BLOCK_CAUSAL_DOCUMENT = 9,
   LCA_BLOCK_SPARSE_UNIFORM = 10,
-  LCA_BLOCK_SPARSE_VARIABLE = 11
+  LCA_BLOCK_SPARSE_VARIABLE = 11,
+  LCA_SLIDING_WINDOW_DOCUMENT = 12   /* the sliding window inside each document */
 } lca_mask_type;
 
 /* Class of one (query tile, key tile) pair; tiles on the last row/column are clipped
@@ -96,14 +98,14 @@ typedef enum {
 typedef struct {
   int32_t type;          /* lca_mask_type                                               */
   int32_t seqlen;        /* S, 1 <= S <= 2^20                                           */
-  int32_t window;        /* SLIDING_WINDOW, GLOBAL_SLIDING: >= 1                        */
+  int32_t window;        /* SLIDING_WINDOW(_DOCUMENT), GLOBAL_SLIDING: >= 1             */
   int32_t num_global;    /* GLOBAL_SLIDING: >= 0                                        */
   int32_t prefix_len;    /* PREFIX_LM: 0 <= prefix_len <= S                             */
   int32_t block;         /* CAUSAL_BLOCKWISE, BLOCK_CAUSAL_DOCUMENT, BLOCK_SPARSE_UNIFORM */
   int32_t base_causal;   /* GLOBAL_SLIDING and block-sparse types (see above)           */
   int32_t num_segments;  /* entries of cu_seqlens minus one; 0 = no segments            */
   const int32_t* cu_seqlens;  /* device int32 [num_segments + 1], 0 = c_0 <= ... <= c_n = S;
-                                 documents (DOCUMENT types, BLOCK_CAUSAL_DOCUMENT,
+                                 documents (DOCUMENT types incl. SLIDING_WINDOW_DOCUMENT, BLOCK_CAUSAL_DOCUMENT,
                                  optional for block-sparse) or segments (SHARED_QUESTION,
                                  segment 0 = question, >= 2 segments)                 */
   int32_t map_heads;     /* block-sparse: H_m = 1, H_kv (GQA: shared in a KV group) or H_q */

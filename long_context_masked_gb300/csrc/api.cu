@@ -77,7 +77,7 @@ bool is_sparse_type(int t) { return t == LCA_BLOCK_SPARSE_UNIFORM || t == LCA_BL
 
 bool needs_segments(int t) {
   return t == LCA_FULL_DOCUMENT || t == LCA_CAUSAL_DOCUMENT || t == LCA_SHARED_QUESTION ||
-         t == LCA_BLOCK_CAUSAL_DOCUMENT;
+         t == LCA_BLOCK_CAUSAL_DOCUMENT || t == LCA_SLIDING_WINDOW_DOCUMENT;
 }
 
 template <typename T>
@@ -97,12 +97,13 @@ bool offsets_ok(const std::vector<int32_t>& v, int n, int S) {
 lca_status validate_desc(const lca_mask_desc* d, int tile_q, int tile_k) {
   if (!d) return LCA_ERR_INVALID_ARG;
   if ((tile_q != 64 && tile_q != 128) || (tile_k != 64 && tile_k != 128)) return LCA_ERR_UNSUPPORTED;
-  if (d->type < LCA_FULL || d->type > LCA_BLOCK_SPARSE_VARIABLE) return LCA_ERR_INVALID_ARG;
+  if (d->type < LCA_FULL || d->type > LCA_SLIDING_WINDOW_DOCUMENT) return LCA_ERR_INVALID_ARG;
   const int S = d->seqlen;
   if (S < 1) return LCA_ERR_INVALID_ARG;
   if (S > kMaxSeqlen) return LCA_ERR_UNSUPPORTED;
   switch (d->type) {
     case LCA_SLIDING_WINDOW:
+    case LCA_SLIDING_WINDOW_DOCUMENT:
       if (d->window < 1) return LCA_ERR_INVALID_ARG;
       break;
     case LCA_GLOBAL_SLIDING:

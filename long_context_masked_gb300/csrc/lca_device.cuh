@@ -407,6 +407,10 @@ __device__ __forceinline__ RowSpan row_span(const MaskDev& m, int i) {
       const int d = seg_find(m.cu, m.num_segments, i);
       r.a0 = __ldg(m.cu + d); r.b0 = i + 1;
     } break;
+    case LCA_SLIDING_WINDOW_DOCUMENT: {
+      const int d = seg_find(m.cu, m.num_segments, i);
+      r.a0 = max(__ldg(m.cu + d), i - m.window + 1); r.b0 = i + 1;
+    } break;
     case LCA_PREFIX_LM: r.b0 = min(S, max(m.prefix_len, i + 1)); break;
     case LCA_SHARED_QUESTION: {
       const int s = seg_find(m.cu, m.num_segments, i);
@@ -481,6 +485,12 @@ __device__ __forceinline__ RowSpan col_span(const MaskDev& m, int j) {
     case LCA_CAUSAL_DOCUMENT: {
       const int d = seg_find(m.cu, m.num_segments, j);
       r.a0 = j; r.b0 = __ldg(m.cu + d + 1);
+    } break;
+    case LCA_SLIDING_WINDOW_DOCUMENT: {   // j <= i < min(end of doc(j), j + w)
+      const int d = seg_find(m.cu, m.num_segments, j);
+      r.a0 = j;
+      r.b0 = static_cast<int>(min(static_cast<long long>(__ldg(m.cu + d + 1)),
+                                  static_cast<long long>(j) + m.window));
     } break;
     case LCA_PREFIX_LM:       // prefix keys are seen by every query
       r.a0 = j < m.prefix_len ? 0 : j; r.b0 = S;

@@ -40,6 +40,7 @@ CAUSAL_BLOCKWISE = 8
 BLOCK_CAUSAL_DOCUMENT = 9
 BLOCK_SPARSE_UNIFORM = 10
 BLOCK_SPARSE_VARIABLE = 11
+SLIDING_WINDOW_DOCUMENT = 12
 
 MASK_NAMES = {
     FULL: "FULL",
@@ -54,6 +55,7 @@ MASK_NAMES = {
     BLOCK_CAUSAL_DOCUMENT: "BLOCK_CAUSAL_DOCUMENT",
     BLOCK_SPARSE_UNIFORM: "BLOCK_SPARSE_UNIFORM",
     BLOCK_SPARSE_VARIABLE: "BLOCK_SPARSE_VARIABLE",
+    SLIDING_WINDOW_DOCUMENT: "SLIDING_WINDOW_DOCUMENT",
 }
 
 # Tile classes written by the mask builder (lca_tile_class).
@@ -230,6 +232,10 @@ def make_desc(mask_type: int, seqlen: int, *, window: int = 4096, num_global: in
         if cu_seqlens is None:
             cu_seqlens = cu_from_lengths(lognormal_doc_lengths(seqlen, doc_seed))
         return MaskDesc(t, seqlen, cu_seqlens=np.asarray(cu_seqlens, np.int32))
+    if t == SLIDING_WINDOW_DOCUMENT:
+        if cu_seqlens is None:
+            cu_seqlens = cu_from_lengths(lognormal_doc_lengths(seqlen, doc_seed))
+        return MaskDesc(t, seqlen, window=window, cu_seqlens=np.asarray(cu_seqlens, np.int32))
     if t == PREFIX_LM:
         return MaskDesc(t, seqlen, prefix_len=seqlen // 4 if prefix_len is None else prefix_len)
     if t == SHARED_QUESTION:

@@ -51,6 +51,12 @@ def n_valid_closed_form(desc, h_m: int = 0) -> int:
         return int((lengths * lengths).sum())
     if t == _in.CAUSAL_DOCUMENT:
         return int((lengths * (lengths + 1) // 2).sum())
+    if t == _in.SLIDING_WINDOW_DOCUMENT:
+        w = desc.window
+        tot = 0
+        for n in lengths.tolist():   # a window of w keys inside every document
+            tot += n * (n + 1) // 2 if n <= w else w * (w + 1) // 2 + (n - w) * w
+        return tot
     if t == _in.PREFIX_LM:
         p = desc.prefix_len
         return p * p + (s * (s + 1) - p * (p + 1)) // 2

@@ -15,6 +15,11 @@ key j, sequence length S):
 * FULL_DOCUMENT / CAUSAL_DOCUMENT: doc(i) == doc(j) [and j <= i], documents
   given by cu_seqlens [§A.4.1 "FULL/CAUSAL DOCUMENT": variable-length
   sequences packed together].
+* SLIDING_WINDOW_DOCUMENT(w): the sliding window inside the query's document,
+  doc(i) == doc(j) and j <= i and i - j < w.  The pages count six regular masks
+  and name FULL, CAUSAL, sliding window and the document variants; this is the
+  plainest sixth (the window's document variant).  Any w >= S reduces to
+  CAUSAL_DOCUMENT, one document to SLIDING_WINDOW.
 * PREFIX_LM(P): j < P or j <= i (bidirectional over the prefix, causal after).
 * SHARED_QUESTION: segment 0 is the question, later segments are answers;
   j <= i and (seg(j) == seg(i) or seg(j) == 0): answers see the question and
@@ -80,6 +85,9 @@ def allowed(desc, h_m: int, i: np.ndarray, j: np.ndarray) -> np.ndarray:
         return _segment_of(desc.cu_seqlens, i) == _segment_of(desc.cu_seqlens, j)
     if t == _in.CAUSAL_DOCUMENT:
         return (_segment_of(desc.cu_seqlens, i) == _segment_of(desc.cu_seqlens, j)) & (j <= i)
+    if t == _in.SLIDING_WINDOW_DOCUMENT:
+        same = _segment_of(desc.cu_seqlens, i) == _segment_of(desc.cu_seqlens, j)
+        return same & (j <= i) & (i - j < desc.window)
     if t == _in.PREFIX_LM:
         return (j < desc.prefix_len) | (j <= i)
     if t == _in.SHARED_QUESTION:

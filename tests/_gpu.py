@@ -79,6 +79,7 @@ def small_descs(s, hq, hkv, seed=0):
         I.make_desc(I.SLIDING_WINDOW, s, window=max(1, s // 5)),
         I.make_desc(I.FULL_DOCUMENT, s, cu_seqlens=cu),
         I.make_desc(I.CAUSAL_DOCUMENT, s, cu_seqlens=cu),
+        I.make_desc(I.SLIDING_WINDOW_DOCUMENT, s, window=max(1, s // 9), cu_seqlens=cu),
         I.make_desc(I.PREFIX_LM, s),
         I.make_desc(I.SHARED_QUESTION, s, question=q_len, answers=answers),
         I.make_desc(I.GLOBAL_SLIDING, s, num_global=max(1, s // 20), window=max(1, s // 6)),

@@ -128,7 +128,8 @@ def _sampled_dq(desc, host, grads, heads, nrows, seed):
 @pytest.mark.parametrize("mask,kw", [(I.FULL, {}), (I.CAUSAL, {}),
                                      (I.SLIDING_WINDOW, {"window": 4096}),
                                      (I.FULL_DOCUMENT, {"doc_seed": 1}),
-                                     (I.CAUSAL_DOCUMENT, {"doc_seed": 1})])
+                                     (I.CAUSAL_DOCUMENT, {"doc_seed": 1}),
+                                     (I.SLIDING_WINDOW_DOCUMENT, {"window": 1024, "doc_seed": 2})])
 def test_dense_regular_full_size(mask, kw):
     s = 16384
     host, dev = make_inputs(1, s, 64, 8, seed=300 + mask)

@@ -103,7 +103,8 @@ def _sampled(desc, b, s, hq, hkv, heads, nrows, seed):
 @pytest.mark.parametrize("mask,kw", [(I.FULL, {}), (I.CAUSAL, {}),
                                      (I.SLIDING_WINDOW, {"window": 4096}),
                                      (I.FULL_DOCUMENT, {"doc_seed": 1}),
-                                     (I.CAUSAL_DOCUMENT, {"doc_seed": 1})])
+                                     (I.CAUSAL_DOCUMENT, {"doc_seed": 1}),
+                                     (I.SLIDING_WINDOW_DOCUMENT, {"window": 1024, "doc_seed": 2})])
 def test_dense_regular_full_size_sampled(mask, kw):
     s = 16384
     desc = I.make_desc(mask, s, **kw)

@@ -32,6 +32,7 @@ def _structured_descs(s, seed):
                    window=int(rng.integers(1, s + 1)), base_causal=1),
         I.MaskDesc(I.CAUSAL_BLOCKWISE, s, block=int(rng.integers(1, s + 2))),
         I.MaskDesc(I.BLOCK_CAUSAL_DOCUMENT, s, block=int(rng.integers(1, 40)), cu_seqlens=cu),
+        I.MaskDesc(I.SLIDING_WINDOW_DOCUMENT, s, window=max(1, w // 2), cu_seqlens=cu),
     ]
     q = int(rng.integers(1, s // 3 + 2))
     rest = s - q
@@ -109,6 +110,12 @@ def test_mask_reductions(s):
     cu = I.cu_from_lengths(I.lognormal_doc_lengths(s, 1, mu=np.log(max(2, s // 3)), lo=1))
     assert _eq(I.MaskDesc(I.BLOCK_CAUSAL_DOCUMENT, s, block=1, cu_seqlens=cu),
                I.MaskDesc(I.CAUSAL_DOCUMENT, s, cu_seqlens=cu))
+    assert _eq(I.MaskDesc(I.SLIDING_WINDOW_DOCUMENT, s, window=s, cu_seqlens=cu),
+               I.MaskDesc(I.CAUSAL_DOCUMENT, s, cu_seqlens=cu))
+    assert _eq(I.MaskDesc(I.SLIDING_WINDOW_DOCUMENT, s, window=w, cu_seqlens=one_doc),
+               I.MaskDesc(I.SLIDING_WINDOW, s, window=w))
+    assert np.array_equal(oracle.materialize_mask(
+        I.MaskDesc(I.SLIDING_WINDOW_DOCUMENT, s, window=1, cu_seqlens=cu)), np.eye(s, dtype=bool))
     if s >= 2:
         assert _eq(I.MaskDesc(I.SHARED_QUESTION, s, cu_seqlens=I.shared_question_cu(1, [s - 1])),
                    causal)
