@@ -41,7 +41,7 @@ extern "C" {
 typedef enum {
   LCA_OK = 0,
   LCA_ERR_INVALID_ARG = 1,   /* null pointer, inconsistent size, bad descriptor         */
-  LCA_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. head_dim != 128)        */
+  LCA_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. head_dim not 64 or 128) */
   LCA_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed                       */
   LCA_ERR_OOM = 4,           /* device allocation for the plan failed                   */
   LCA_ERR_TIMEOUT = 5,       /* a bounded device-side wait ran out                      */
@@ -166,7 +166,7 @@ lca_status lca_plan_export(const lca_plan* plan, uint8_t* cls, int32_t* rowptr, 
 void lca_plan_destroy(lca_plan* plan);
 
 /* Forward: O (bf16) and LSE (fp32, natural log) for all heads and rows.
- * Requires head_dim == 128, plan tile_q == 128, tile_k == 128, plan seqlen ==
+ * Requires head_dim 128 or 64, plan tile_q == 128, tile_k == 128, plan seqlen ==
  * shape->seqlen, plan map_heads in {1, h_kv, h_q}.  softmax_scale <= 0 means
  * 1/sqrt(head_dim). */
 lca_status lca_attn_fwd(const lca_plan* plan, const lca_shape* shape, const void* q,

@@ -56,12 +56,12 @@ EncodeTiledFn encode_fn() {
 // Tensor map of a [B, S, H, 128] bf16 tensor (row stride in elements); a box is
 // `box_rows` positions x one head x 64 elements, 128-byte swizzled (one half of a row).
 bool make_tmap_bshd(CUtensorMap* m, const void* ptr, int batch, int seqlen, int heads,
-                    int64_t row_stride, int box_rows) {
+                    int64_t row_stride, int box_rows, int head_dim = kHeadDim) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
-  cuuint64_t dims[4] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(heads),
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(heads),
                         static_cast<cuuint64_t>(seqlen), static_cast<cuuint64_t>(batch)};
-  cuuint64_t strides[3] = {static_cast<cuuint64_t>(kHeadDim) * 2,
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(head_dim) * 2,
                            static_cast<cuuint64_t>(row_stride) * 2,
                            static_cast<cuuint64_t>(row_stride) * 2 * seqlen};
   cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(box_rows), 1};
@@ -396,9 +396,9 @@ lca_status check_shape(const lca_plan* p, const lca_shape* s) {
   if (s->batch < 1 || s->seqlen < 1 || s->h_q < 1 || s->h_kv < 1 || s->head_dim < 1)
     return LCA_ERR_INVALID_ARG;
   if (s->h_q % s->h_kv != 0) return LCA_ERR_INVALID_ARG;
-  if (s->head_dim != kHeadDim) return LCA_ERR_UNSUPPORTED;
-  const int64_t q_min = static_cast<int64_t>(s->h_q) * kHeadDim;
-  const int64_t k_min = static_cast<int64_t>(s->h_kv) * kHeadDim;
+  if (s->head_dim != 128 && s->head_dim != 64) return LCA_ERR_UNSUPPORTED;
+  const int64_t q_min = static_cast<int64_t>(s->h_q) * s->head_dim;
+  const int64_t k_min = static_cast<int64_t>(s->h_kv) * s->head_dim;
   if (s->q_row_stride < q_min || s->o_row_stride < q_min || s->k_row_stride < k_min ||
       s->v_row_stride < k_min)
     return LCA_ERR_INVALID_ARG;
@@ -427,6 +427,7 @@ AttnDims make_dims(const lca_plan* p, const lca_shape* s, float softmax_scale) {
   d.kv_per_map = p->info.map_heads <= s->h_kv ? s->h_kv / p->info.map_heads : 0;
   d.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(s->head_dim));
   d.scale_log2 = d.scale * 1.4426950408889634f;
+  d.head_dim = s->head_dim;
   // 16 consecutive work items per launch-order group: MHA kernels then share K/V
   // (Q/dO) tiles in L2 across the resident CTAs; GQA is indifferent to it.
   d.chunk = 16;
@@ -446,9 +447,9 @@ lca_status lca_attn_fwd(const lca_plan* plan, const lca_shape* shape, const void
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return LCA_ERR_INVALID_ARG;
   CUtensorMap tq, tk, tv;
-  if (!make_tmap_bshd(&tq, q, shape->batch, shape->seqlen, shape->h_q, shape->q_row_stride, 128) ||
-      !make_tmap_bshd(&tk, k, shape->batch, shape->seqlen, shape->h_kv, shape->k_row_stride, 128) ||
-      !make_tmap_bshd(&tv, v, shape->batch, shape->seqlen, shape->h_kv, shape->v_row_stride, 128))
+  if (!make_tmap_bshd(&tq, q, shape->batch, shape->seqlen, shape->h_q, shape->q_row_stride, 128, shape->head_dim) ||
+      !make_tmap_bshd(&tk, k, shape->batch, shape->seqlen, shape->h_kv, shape->k_row_stride, 128, shape->head_dim) ||
+      !make_tmap_bshd(&tv, v, shape->batch, shape->seqlen, shape->h_kv, shape->v_row_stride, 128, shape->head_dim))
     return LCA_ERR_CUDA;
   FwdArgs a;
   a.dims = make_dims(plan, shape, softmax_scale);
@@ -488,10 +489,10 @@ lca_status lca_attn_bwd(const lca_plan* plan, const lca_shape* shape, const void
     if (!aligned16(ptr)) return LCA_ERR_INVALID_ARG;
   if (ws_bytes < lca_attn_bwd_workspace(plan, shape, flags)) return LCA_ERR_INVALID_ARG;
   CUtensorMap tq, tk, tv, tdo;
-  if (!make_tmap_bshd(&tq, q, shape->batch, shape->seqlen, shape->h_q, shape->q_row_stride, 128) ||
-      !make_tmap_bshd(&tk, k, shape->batch, shape->seqlen, shape->h_kv, shape->k_row_stride, 128) ||
-      !make_tmap_bshd(&tv, v, shape->batch, shape->seqlen, shape->h_kv, shape->v_row_stride, 128) ||
-      !make_tmap_bshd(&tdo, dout, shape->batch, shape->seqlen, shape->h_q, shape->o_row_stride, 128))
+  if (!make_tmap_bshd(&tq, q, shape->batch, shape->seqlen, shape->h_q, shape->q_row_stride, 128, shape->head_dim) ||
+      !make_tmap_bshd(&tk, k, shape->batch, shape->seqlen, shape->h_kv, shape->k_row_stride, 128, shape->head_dim) ||
+      !make_tmap_bshd(&tv, v, shape->batch, shape->seqlen, shape->h_kv, shape->v_row_stride, 128, shape->head_dim) ||
+      !make_tmap_bshd(&tdo, dout, shape->batch, shape->seqlen, shape->h_q, shape->o_row_stride, 128, shape->head_dim))
     return LCA_ERR_CUDA;
   BwdArgs a;
   a.dims = make_dims(plan, shape, softmax_scale);

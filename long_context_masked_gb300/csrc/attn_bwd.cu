@@ -31,20 +31,20 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BN = 128;
-constexpr int HD = 128;
-constexpr uint32_t TILE = BM * HD * 2;
-constexpr uint32_t HALF = TILE / 2;
+constexpr uint32_t HALF = BM * 64 * 2;   // one 128-byte-swizzled 64-column half, 16 KB
 constexpr float LOG2E = 1.4426950408889634f;
 
 // ------------------------------------------------------------------ preprocess
 
+template <int HD>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(BwdArgs a) {
-  // One 16-thread group per (b, i, h) row of the padded workspace, h fastest so the O
+  constexpr int TPR = HD / 8;   // threads per row, 8 elements each
+  // One TPR-thread group per (b, i, h) row of the padded workspace, h fastest so the O
   // and dO reads coalesce; rows i >= S only write the padding values.
   const int S = a.dims.seqlen, hq = a.dims.h_q;
   const int64_t rows = static_cast<int64_t>(a.dims.batch) * a.s_pad * hq;
-  const int64_t r = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 4;
-  const int part = threadIdx.x & 15;
+  const int64_t r = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) / TPR;
+  const int part = threadIdx.x % TPR;
   const int h = static_cast<int>(r % hq);
   const int64_t bi = r / hq;
   const int64_t b = bi / a.s_pad, i = bi % a.s_pad;
@@ -65,7 +65,7 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(BwdArgs a) {
     }
   }
 #pragma unroll
-  for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
+  for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
   if (part == 0 && r < rows) {
     const int64_t w = (b * hq + h) * a.s_pad + i;
     float l2 = INFINITY;
@@ -103,20 +103,44 @@ __device__ __forceinline__ void ds_half(const uint32_t (&sr)[64], const uint32_t
   }
 }
 
-// Read 64 fp32 accumulator columns of this thread's lane, scale, store 64 bf16.
+// N consecutive 32-bit TMEM columns (N = 16, 32 or 64) of this thread's lane.
+template <int N>
+__device__ __forceinline__ void tmem_ldn(uint32_t taddr, uint32_t (&r)[N]) {
+  static_assert(N == 32 || N == 64, "32 or 64 columns");
+  if constexpr (N == 64) tmem_ld64(taddr, r); else tmem_ld32(taddr, r);
+}
+template <int N>
+__device__ __forceinline__ void tmem_stn(uint32_t taddr, const uint32_t (&r)[N]) {
+  static_assert(N == 16 || N == 32, "16 or 32 columns");
+  if constexpr (N == 32) {
+    tmem_st32(taddr, r);
+  } else {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};\n\t"
+        "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15])
+        : "memory");
+  }
+}
+
+// Read N fp32 accumulator columns of this thread's lane, scale, store N bf16.
+template <int N>
 __device__ __forceinline__ void store_acc_half(uint32_t taddr, bool have, float scale,
                                                __nv_bfloat16* dst, bool write) {
-  uint32_t r[64];
+  uint32_t r[N];
   if (have) {
-    tmem_ld64(taddr, r);
+    tmem_ldn<N>(taddr, r);
   } else {
 #pragma unroll
-    for (int x = 0; x < 64; ++x) r[x] = 0u;
+    for (int x = 0; x < N; ++x) r[x] = 0u;
   }
   if (write) {
     uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
-    for (int v = 0; v < 8; ++v) {
+    for (int v = 0; v < N / 8; ++v) {
       const int x = v * 8;
       uint4 w;
       w.x = pack_bf16x2(__uint_as_float(r[x + 0]) * scale, __uint_as_float(r[x + 1]) * scale);
@@ -146,16 +170,27 @@ __device__ __forceinline__ void store_acc_half(uint32_t taddr, bool have, float 
 constexpr int KV_QST = 3;
 constexpr int KV_DOST = 2;
 constexpr uint32_t ROWV = BM * 4;                   // one step's LSE2 or D values
-constexpr uint32_t KV_OFF_K = 0;
-constexpr uint32_t KV_OFF_V = TILE;
-constexpr uint32_t KV_OFF_Q = 2 * TILE;
-constexpr uint32_t KV_OFF_DO = KV_OFF_Q + KV_QST * TILE;
-constexpr uint32_t KV_OFF_LSE = KV_OFF_DO + KV_DOST * TILE;   // one per Q stage
-constexpr uint32_t KV_OFF_D = KV_OFF_LSE + KV_QST * ROWV;     // one per dO stage
-constexpr uint32_t KV_OFF_BAR = KV_OFF_D + KV_DOST * ROWV;
-constexpr uint32_t KV_SMEM = KV_OFF_BAR + 256;                // the dynamic base is 1024-aligned
-static_assert(KV_SMEM <= 232448, "dynamic shared memory above the 227 KB per-CTA limit");
 constexpr uint32_t KV_TM_S = 0, KV_TM_DP = 128, KV_TM_DV = 256, KV_TM_DK = 384;
+
+// Head-dim dependent layouts (head_dim 128 or 64): a Q/K/V/dO tile is 128 rows x HD
+// columns in HD / 64 swizzled halves; shared-memory offsets from a 1024-aligned base.
+template <int HD_>
+struct BwdCfg {
+  static constexpr int HD = HD_;
+  static constexpr int NH = HD / 64;
+  static constexpr int ACOLS = HD / 2;      // accumulator columns per thread (2 per lane)
+  static constexpr uint32_t TILE = BM * HD * 2;
+  static constexpr uint32_t KV_OFF_K = 0;
+  static constexpr uint32_t KV_OFF_V = TILE;
+  static constexpr uint32_t KV_OFF_Q = 2 * TILE;
+  static constexpr uint32_t KV_OFF_DO = KV_OFF_Q + KV_QST * TILE;
+  static constexpr uint32_t KV_OFF_LSE = KV_OFF_DO + KV_DOST * TILE;   // one per Q stage
+  static constexpr uint32_t KV_OFF_D = KV_OFF_LSE + KV_QST * ROWV;     // one per dO stage
+  static constexpr uint32_t KV_OFF_BAR = KV_OFF_D + KV_DOST * ROWV;
+  static constexpr uint32_t KV_SMEM = KV_OFF_BAR + 256;
+  static_assert(HD == 64 || HD == 128, "head_dim 64 or 128");
+  static_assert(KV_SMEM <= 232448, "dynamic shared memory above the 227 KB per-CTA limit");
+};
 
 struct KvBars {
   uint64_t kv_full;
@@ -205,10 +240,17 @@ struct ColWalk {
   }
 };
 
+template <int HD_>
 __global__ void __launch_bounds__(KV_THREADS, 1)
 bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                 BwdArgs a) {
+  using C = BwdCfg<HD_>;
+  constexpr int HD = C::HD, NH = C::NH, ACOLS = C::ACOLS;
+  constexpr uint32_t TILE = C::TILE;
+  constexpr uint32_t KV_OFF_K = C::KV_OFF_K, KV_OFF_V = C::KV_OFF_V, KV_OFF_Q = C::KV_OFF_Q,
+                     KV_OFF_DO = C::KV_OFF_DO, KV_OFF_LSE = C::KV_OFF_LSE, KV_OFF_D = C::KV_OFF_D,
+                     KV_OFF_BAR = C::KV_OFF_BAR;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t base_u32 = smem_u32(smem_raw);
   if (base_u32 & 1023u) {
@@ -275,7 +317,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       mbar_arrive_expect_tx(&bar.kv_full, 2 * TILE);
-      for (int c = 0; c < 2; ++c) {
+      for (int c = 0; c < NH; ++c) {
         tma_load_4d(base + KV_OFF_K + c * HALF, &tm_k, &bar.kv_full, c * 64, hk, kt * BN, b);
         tma_load_4d(base + KV_OFF_V + c * HALF, &tm_v, &bar.kv_full, c * 64, hk, kt * BN, b);
       }
@@ -283,15 +325,15 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       ColWalk ahead = walk;   // L2 prefetch of the Q tile KV_QST steps ahead
       int ha, qa, ca;
       for (int k = 0; k < KV_QST && ahead.next(ha, qa, ca); ++k)
-        for (int c = 0; c < 2; ++c) tma_prefetch_l2_4d(&tm_q, c * 64, ha, qa * BM, b);
+        for (int c = 0; c < NH; ++c) tma_prefetch_l2_4d(&tm_q, c * 64, ha, qa * BM, b);
       while (walk.next(h, qt, cls)) {
         const int st = t % KV_QST;
         const uint32_t ph = (t / KV_QST) & 1;
         if (ahead.next(ha, qa, ca))
-          for (int c = 0; c < 2; ++c) tma_prefetch_l2_4d(&tm_q, c * 64, ha, qa * BM, b);
+          for (int c = 0; c < NH; ++c) tma_prefetch_l2_4d(&tm_q, c * 64, ha, qa * BM, b);
         if (t >= KV_QST) mbar_wait(&bar.q_empty[st], ph ^ 1u, wc);
         mbar_arrive_expect_tx(&bar.q_full[st], TILE + ROWV);
-        for (int c = 0; c < 2; ++c)
+        for (int c = 0; c < NH; ++c)
           tma_load_4d(base + KV_OFF_Q + st * TILE + c * HALF, &tm_q, &bar.q_full[st], c * 64, h,
                       qt * BM, b);
         bulk_load(base + KV_OFF_LSE + st * ROWV,
@@ -312,15 +354,15 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       ColWalk ahead = walk;   // L2 prefetch of the dO tile KV_QST steps ahead
       int ha, qa, ca;
       for (int k = 0; k < KV_QST && ahead.next(ha, qa, ca); ++k)
-        for (int c = 0; c < 2; ++c) tma_prefetch_l2_4d(&tm_do, c * 64, ha, qa * BM, b);
+        for (int c = 0; c < NH; ++c) tma_prefetch_l2_4d(&tm_do, c * 64, ha, qa * BM, b);
       while (walk.next(h, qt, cls)) {
         const int st = t % KV_DOST;
         const uint32_t ph = (t / KV_DOST) & 1;
         if (ahead.next(ha, qa, ca))
-          for (int c = 0; c < 2; ++c) tma_prefetch_l2_4d(&tm_do, c * 64, ha, qa * BM, b);
+          for (int c = 0; c < NH; ++c) tma_prefetch_l2_4d(&tm_do, c * 64, ha, qa * BM, b);
         if (t >= KV_DOST) mbar_wait(&bar.do_empty[st], ph ^ 1u, wc);
         mbar_arrive_expect_tx(&bar.do_full[st], TILE + ROWV);
-        for (int c = 0; c < 2; ++c)
+        for (int c = 0; c < NH; ++c)
           tma_load_4d(base + KV_OFF_DO + st * TILE + c * HALF, &tm_do, &bar.do_full[st], c * 64,
                       h, qt * BM, b);
         bulk_load(base + KV_OFF_D + st * ROWV,
@@ -489,9 +531,10 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       tc_fence_after();
     }
     const int64_t roff = (static_cast<int64_t>(b) * S + j) * a.k_row_stride +
-                         static_cast<int64_t>(hk) * HD + half * 64;
-    store_acc_half(lane_addr + KV_TM_DV, t > 0, 1.f, a.dv + roff, jvalid);
-    store_acc_half(lane_addr + KV_TM_DK, t > 0, dm.scale, a.dk + roff, jvalid);
+                         static_cast<int64_t>(hk) * HD + half * ACOLS;
+    const uint32_t acc_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + half * ACOLS;
+    store_acc_half<ACOLS>(acc_addr + KV_TM_DV, t > 0, 1.f, a.dv + roff, jvalid);
+    store_acc_half<ACOLS>(acc_addr + KV_TM_DK, t > 0, dm.scale, a.dk + roff, jvalid);
   }
 
   tc_fence_before();
@@ -509,12 +552,17 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 // memory it frees gives K (held from S to dQ) a fourth stage.
 constexpr int DQ_KST = 4;                        // K stages (K is held until the dQ MMA)
 constexpr int DQ_VST = 2;                        // V stages (V is released after dP)
-constexpr uint32_t DQ_OFF_Q = 0;
-constexpr uint32_t DQ_OFF_K = TILE;
-constexpr uint32_t DQ_OFF_V = DQ_OFF_K + DQ_KST * TILE;
-constexpr uint32_t DQ_OFF_BAR = DQ_OFF_V + DQ_VST * TILE;
-constexpr uint32_t DQ_SMEM = DQ_OFF_BAR + 256;    // the dynamic base is 1024-aligned
-static_assert(DQ_SMEM <= 232448, "dynamic shared memory above the 227 KB per-CTA limit");
+
+template <int HD_>
+struct DqCfg {
+  static constexpr uint32_t TILE = BwdCfg<HD_>::TILE;
+  static constexpr uint32_t DQ_OFF_Q = 0;
+  static constexpr uint32_t DQ_OFF_K = TILE;
+  static constexpr uint32_t DQ_OFF_V = DQ_OFF_K + DQ_KST * TILE;
+  static constexpr uint32_t DQ_OFF_BAR = DQ_OFF_V + DQ_VST * TILE;
+  static constexpr uint32_t DQ_SMEM = DQ_OFF_BAR + 256;   // the dynamic base is 1024-aligned
+  static_assert(DQ_SMEM <= 232448, "dynamic shared memory above the 227 KB per-CTA limit");
+};
 constexpr uint32_t DQ_TM_S = 0, DQ_TM_DP = 128, DQ_TM_DQ = 256, DQ_TM_DS = 384, DQ_TM_DO = 448;
 
 struct DqBars {
@@ -525,10 +573,18 @@ struct DqBars {
   int abort;
 };
 
+template <int HD_>
 __global__ void __launch_bounds__(DQ_THREADS, 1)
 bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
               BwdArgs a) {
+  using C = BwdCfg<HD_>;
+  using D = DqCfg<HD_>;
+  constexpr int HD = C::HD, NH = C::NH, ACOLS = C::ACOLS;
+  constexpr uint32_t TILE = C::TILE;
+  constexpr uint32_t DQ_OFF_Q = D::DQ_OFF_Q, DQ_OFF_K = D::DQ_OFF_K, DQ_OFF_V = D::DQ_OFF_V,
+                     DQ_OFF_BAR = D::DQ_OFF_BAR;
+  constexpr int DOC = HD / 4;   // TMEM columns of this thread's half row of dO (bf16 pairs)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t base_u32 = smem_u32(smem_raw);
   if (base_u32 & 1023u) {   // the swizzled tiles need a 1024-byte-aligned base
@@ -586,18 +642,18 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   if (warp == WARP_PRODUCER) {
     if (lane == 0) {
       mbar_arrive_expect_tx(&bar.q_full, TILE);
-      for (int c = 0; c < 2; ++c)
+      for (int c = 0; c < NH; ++c)
         tma_load_4d(base + DQ_OFF_Q + c * HALF, &tm_q, &bar.q_full, c * 64, h, qt * BM, b);
       for (int n = 0; n < n_tiles; ++n) {
         const int kt = __ldg(pl.kt_idx + tile(n));
         const int st = n % DQ_KST;
         if (n + DQ_KST < n_tiles) {
           const int ka = __ldg(pl.kt_idx + tile(n + DQ_KST));
-          for (int c = 0; c < 2; ++c) tma_prefetch_l2_4d(&tm_k, c * 64, hk, ka * BN, b);
+          for (int c = 0; c < NH; ++c) tma_prefetch_l2_4d(&tm_k, c * 64, hk, ka * BN, b);
         }
         if (n >= DQ_KST) mbar_wait(&bar.k_empty[st], (n / DQ_KST - 1) & 1, wc);
         mbar_arrive_expect_tx(&bar.k_full[st], TILE);
-        for (int c = 0; c < 2; ++c)
+        for (int c = 0; c < NH; ++c)
           tma_load_4d(base + DQ_OFF_K + st * TILE + c * HALF, &tm_k, &bar.k_full[st], c * 64, hk,
                       kt * BN, b);
       }
@@ -616,11 +672,11 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const int st = n % DQ_VST;
         if (n + DQ_VST < n_tiles) {
           const int ka = __ldg(pl.kt_idx + tile(n + DQ_VST));
-          for (int c = 0; c < 2; ++c) tma_prefetch_l2_4d(&tm_v, c * 64, hk, ka * BN, b);
+          for (int c = 0; c < NH; ++c) tma_prefetch_l2_4d(&tm_v, c * 64, hk, ka * BN, b);
         }
         if (n >= DQ_VST) mbar_wait(&bar.v_empty[st], (n / DQ_VST - 1) & 1, wc);
         mbar_arrive_expect_tx(&bar.v_full[st], TILE);
-        for (int c = 0; c < 2; ++c)
+        for (int c = 0; c < NH; ++c)
           tma_load_4d(base + DQ_OFF_V + st * TILE + c * HALF, &tm_v, &bar.v_full[st], c * 64, hk,
                       kt * BN, b);
       }
@@ -707,22 +763,23 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     const float lse2 = __ldg(a.lse2 + rowi);
     const float dsum = __ldg(a.dsum + rowi);
     const int64_t roff = (static_cast<int64_t>(b) * S + i) * a.o_row_stride +
-                         static_cast<int64_t>(h) * HD + half * 64;
+                         static_cast<int64_t>(h) * HD + half * ACOLS;
     {
-      // this thread's half row of dO (64 bf16) into TMEM columns [DQ_TM_DO + 32 half, +32)
-      uint32_t v[32];
+      // this thread's half row of dO (HD / 2 bf16) into TMEM columns
+      // [DQ_TM_DO + DOC half, + DOC)
+      uint32_t v[DOC];
       if (valid) {
         const uint4* src = reinterpret_cast<const uint4*>(a.dout + roff);
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
+        for (int u = 0; u < DOC / 4; ++u) {
           const uint4 w = __ldg(src + u);
           v[4 * u] = w.x; v[4 * u + 1] = w.y; v[4 * u + 2] = w.z; v[4 * u + 3] = w.w;
         }
       } else {
 #pragma unroll
-        for (int u = 0; u < 32; ++u) v[u] = 0u;
+        for (int u = 0; u < DOC; ++u) v[u] = 0u;
       }
-      tmem_st32(quarter_addr + DQ_TM_DO + half * 32, v);
+      tmem_stn<DOC>(quarter_addr + DQ_TM_DO + half * DOC, v);
       tc_fence_before();
       mbar_arrive(&bar.do_ready);
     }
@@ -755,7 +812,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       __syncwarp();
       tc_fence_after();
     }
-    store_acc_half(lane_addr + DQ_TM_DQ, n_tiles > 0, dm.scale, a.dq + roff, valid);
+    store_acc_half<ACOLS>(quarter_addr + DQ_TM_DQ + half * ACOLS, n_tiles > 0, dm.scale,
+                          a.dq + roff, valid);
   }
 
   tc_fence_before();
@@ -770,8 +828,36 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 
 cudaError_t launch_bwd_preprocess(const BwdArgs& a, cudaStream_t st) {
   const int64_t rows = static_cast<int64_t>(a.dims.batch) * a.s_pad * a.dims.h_q;
-  const int64_t blocks = (rows * 16 + 255) / 256;
-  bwd_preprocess_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(a);
+  const int tpr = a.dims.head_dim / 8;
+  const int64_t blocks = (rows * tpr + 255) / 256;
+  if (a.dims.head_dim == 64)
+    bwd_preprocess_kernel<64><<<static_cast<unsigned>(blocks), 256, 0, st>>>(a);
+  else
+    bwd_preprocess_kernel<128><<<static_cast<unsigned>(blocks), 256, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+template <int HD>
+static cudaError_t launch_dkdv_hd(const CUtensorMap& tq, const CUtensorMap& tk,
+                                  const CUtensorMap& tv, const CUtensorMap& tdo, const BwdArgs& a,
+                                  int n_blocks, cudaStream_t st) {
+  constexpr uint32_t smem = BwdCfg<HD>::KV_SMEM;
+  cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_kernel<HD>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  bwd_dkdv_kernel<HD><<<n_blocks, KV_THREADS, smem, st>>>(tq, tk, tv, tdo, a);
+  return cudaGetLastError();
+}
+
+template <int HD>
+static cudaError_t launch_dq_hd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                const CUtensorMap& tdo, const BwdArgs& a, int n_blocks,
+                                cudaStream_t st) {
+  constexpr uint32_t smem = DqCfg<HD>::DQ_SMEM;
+  cudaError_t e = cudaFuncSetAttribute(bwd_dq_kernel<HD>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  bwd_dq_kernel<HD><<<n_blocks, DQ_THREADS, smem, st>>>(tq, tk, tv, tdo, a);
   return cudaGetLastError();
 }
 
@@ -779,22 +865,16 @@ cudaError_t launch_bwd_dkdv(const CUtensorMap& tq, const CUtensorMap& tk, const 
                             const CUtensorMap& tdo, const BwdArgs& a, int n_blocks,
                             cudaStream_t st) {
   if (n_blocks == 0) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, KV_SMEM);
-  if (e != cudaSuccess) return e;
-  bwd_dkdv_kernel<<<n_blocks, KV_THREADS, KV_SMEM, st>>>(tq, tk, tv, tdo, a);
-  return cudaGetLastError();
+  if (a.dims.head_dim == 64) return launch_dkdv_hd<64>(tq, tk, tv, tdo, a, n_blocks, st);
+  return launch_dkdv_hd<128>(tq, tk, tv, tdo, a, n_blocks, st);
 }
 
 cudaError_t launch_bwd_dq(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const CUtensorMap& tdo, const BwdArgs& a, int n_blocks,
                           cudaStream_t st) {
   if (n_blocks == 0) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(bwd_dq_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, DQ_SMEM);
-  if (e != cudaSuccess) return e;
-  bwd_dq_kernel<<<n_blocks, DQ_THREADS, DQ_SMEM, st>>>(tq, tk, tv, tdo, a);
-  return cudaGetLastError();
+  if (a.dims.head_dim == 64) return launch_dq_hd<64>(tq, tk, tv, tdo, a, n_blocks, st);
+  return launch_dq_hd<128>(tq, tk, tv, tdo, a, n_blocks, st);
 }
 
 }  // namespace lca

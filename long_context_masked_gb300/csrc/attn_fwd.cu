@@ -21,7 +21,7 @@
 //               (exact after the final 1/l normalisation), then the epilogue.
 // Keeping P in TMEM matters on this part: an M = N = 128 MMA with both operands in
 // shared memory reads 128 B/clk, the whole shared-memory bandwidth of the SM.
-// Tile = 128 x 128, head_dim = 128.  All waits are bounded.
+// Tile = 128 x 128, head_dim 128 or 64.  All waits are bounded.
 #include <cuda_runtime.h>
 
 #include "attn_kernels.h"
@@ -33,9 +33,7 @@ namespace {
 
 constexpr int BM = 128;              // query rows per tile
 constexpr int BN = 128;              // keys per tile
-constexpr int HD = 128;              // head dim
-constexpr uint32_t TILE_BYTES = BM * HD * 2;   // 32 KB, two 128-byte-swizzled halves
-constexpr uint32_t HALF_BYTES = TILE_BYTES / 2;
+constexpr uint32_t HALF_BYTES = BM * 64 * 2;   // one 128-byte-swizzled 64-column half, 16 KB
 constexpr float RESCALE_THRESHOLD = 8.0f;      // log2 units
 
 constexpr int NUM_THREADS = 352;     // 8 softmax warps, MMA issuer, K and V producers
@@ -47,18 +45,38 @@ constexpr int KST = 3;                // K stages
 constexpr int VST = 3;                // V stages
 constexpr int NSB = 3;                // S buffers in TMEM
 
-// shared memory map (offsets from a 1024-aligned base)
-constexpr uint32_t OFF_Q = 0;
-constexpr uint32_t OFF_K = OFF_Q + TILE_BYTES;          // KST stages
-constexpr uint32_t OFF_V = OFF_K + KST * TILE_BYTES;    // VST stages
-constexpr uint32_t OFF_BAR = OFF_V + VST * TILE_BYTES;
-constexpr uint32_t OFF_RED = OFF_BAR + 256;           // row-max / row-sum exchange
-constexpr uint32_t SMEM_BYTES = OFF_RED + 2 * 2 * BM * 4;   // base is 1024-aligned
-static_assert(SMEM_BYTES <= 232448, "dynamic shared memory above the 227 KB per-CTA limit");
+// Head-dim dependent layout (head_dim 128 or 64).  A Q/K/V tile is 128 rows x HD
+// columns, stored as HD / 64 swizzled halves; shared memory offsets from a 1024-aligned
+// base.
+template <int HD_>
+struct Cfg {
+  static constexpr int HD = HD_;
+  static constexpr int NH = HD / 64;                          // swizzled halves per tile
+  static constexpr uint32_t TILE_BYTES = BM * HD * 2;
+  static constexpr uint32_t OFF_Q = 0;
+  static constexpr uint32_t OFF_K = OFF_Q + TILE_BYTES;       // KST stages
+  static constexpr uint32_t OFF_V = OFF_K + KST * TILE_BYTES; // VST stages
+  static constexpr uint32_t OFF_BAR = OFF_V + VST * TILE_BYTES;
+  static constexpr uint32_t OFF_RED = OFF_BAR + 256;          // row-max / row-sum exchange
+  static constexpr uint32_t SMEM_BYTES = OFF_RED + 2 * 2 * BM * 4;
+  static constexpr int OCOLS = HD / 2;                        // O columns per softmax thread
+  static_assert(HD == 64 || HD == 128, "head_dim 64 or 128");
+  static_assert(SMEM_BYTES <= 232448, "dynamic shared memory above the 227 KB per-CTA limit");
+};
 
 // TMEM columns
 constexpr uint32_t TM_S0 = 0, TM_O = NSB * BN, TM_COLS = 512;
-static_assert(TM_O + HD <= TM_COLS, "TMEM columns");
+static_assert(TM_O + 128 <= TM_COLS, "TMEM columns");
+
+// N consecutive 32-bit TMEM columns (N = 32 or 64) of this thread's lane.
+template <int N>
+__device__ __forceinline__ void tmem_ldn(uint32_t taddr, uint32_t (&r)[N]) {
+  if constexpr (N == 64) tmem_ld64(taddr, r); else tmem_ld32(taddr, r);
+}
+template <int N>
+__device__ __forceinline__ void tmem_stn(uint32_t taddr, const uint32_t (&r)[N]) {
+  if constexpr (N == 64) tmem_st64(taddr, r); else tmem_st32(taddr, r);
+}
 
 struct Bars {
   uint64_t q_full;
@@ -76,9 +94,16 @@ __device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile, int kk) {
   return desc_mnmajor(tile, kk, HALF_BYTES);
 }
 
+template <int HD_>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, FwdArgs a) {
+  using C = Cfg<HD_>;
+  constexpr int HD = C::HD;
+  constexpr uint32_t TILE_BYTES = C::TILE_BYTES;
+  constexpr uint32_t OFF_Q = C::OFF_Q, OFF_K = C::OFF_K, OFF_V = C::OFF_V, OFF_BAR = C::OFF_BAR,
+                     OFF_RED = C::OFF_RED;
+  constexpr int OCOLS = C::OCOLS;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t base_u32 = smem_u32(smem_raw);
   if (base_u32 & 1023u) {   // the swizzled tiles need a 1024-byte-aligned base
@@ -144,18 +169,18 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       mbar_arrive_expect_tx(&bar.q_full, TILE_BYTES);
-      for (int c = 0; c < 2; ++c)
+      for (int c = 0; c < C::NH; ++c)
         tma_load_4d(base + OFF_Q + c * HALF_BYTES, &tm_q, &bar.q_full, c * 64, h, qt * BM, b);
       for (int n = 0; n < n_tiles; ++n) {
         const int kt = __ldg(pl.kt_idx + beg + n);
         const int ks = n % KST;
         if (n + KST < n_tiles) {   // L2 prefetch one ring ahead
           const int ka = __ldg(pl.kt_idx + beg + n + KST);
-          for (int c = 0; c < 2; ++c) tma_prefetch_l2_4d(&tm_k, c * 64, hk, ka * BN, b);
+          for (int c = 0; c < C::NH; ++c) tma_prefetch_l2_4d(&tm_k, c * 64, hk, ka * BN, b);
         }
         if (n >= KST) mbar_wait(&bar.k_empty[ks], (n / KST - 1) & 1, wc);
         mbar_arrive_expect_tx(&bar.k_full[ks], TILE_BYTES);
-        for (int c = 0; c < 2; ++c)
+        for (int c = 0; c < C::NH; ++c)
           tma_load_4d(base + OFF_K + ks * TILE_BYTES + c * HALF_BYTES, &tm_k, &bar.k_full[ks],
                       c * 64, hk, kt * BN, b);
       }
@@ -171,11 +196,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const int vs = n % VST;
         if (n + VST < n_tiles) {
           const int ka = __ldg(pl.kt_idx + beg + n + VST);
-          for (int c = 0; c < 2; ++c) tma_prefetch_l2_4d(&tm_v, c * 64, hk, ka * BN, b);
+          for (int c = 0; c < C::NH; ++c) tma_prefetch_l2_4d(&tm_v, c * 64, hk, ka * BN, b);
         }
         if (n >= VST) mbar_wait(&bar.v_empty[vs], (n / VST - 1) & 1, wc);
         mbar_arrive_expect_tx(&bar.v_full[vs], TILE_BYTES);
-        for (int c = 0; c < 2; ++c)
+        for (int c = 0; c < C::NH; ++c)
           tma_load_4d(base + OFF_V + vs * TILE_BYTES + c * HALF_BYTES, &tm_v, &bar.v_full[vs],
                       c * 64, hk, kt * BN, b);
       }
@@ -295,11 +320,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         __syncwarp();
         tc_fence_after();
         const float f = rescale ? alpha : 1.f;
-        uint32_t o[64];
-        tmem_ld64(lane_addr + TM_O, o);
+        uint32_t o[OCOLS];
+        tmem_ldn<OCOLS>(quarter_addr + TM_O + half * OCOLS, o);
 #pragma unroll
-        for (int x = 0; x < 64; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * f);
-        tmem_st64(lane_addr + TM_O, o);
+        for (int x = 0; x < OCOLS; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * f);
+        tmem_stn<OCOLS>(quarter_addr + TM_O + half * OCOLS, o);
       }
       const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
       float ls[8];
@@ -335,19 +360,19 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     named_bar_sync(BAR_SOFTMAX, SOFTMAX_THREADS);
     const float l_tot = l_run + red[(pe * 2 + (half ^ 1)) * BM + t];
     const float inv = (l_tot > 0.f) ? 1.f / l_tot : 0.f;
-    uint32_t o[64];
+    uint32_t o[OCOLS];
     if (n_tiles > 0) {
-      tmem_ld64(lane_addr + TM_O, o);
+      tmem_ldn<OCOLS>(quarter_addr + TM_O + half * OCOLS, o);
     } else {
 #pragma unroll
-      for (int x = 0; x < 64; ++x) o[x] = 0u;
+      for (int x = 0; x < OCOLS; ++x) o[x] = 0u;
     }
     if (i < S) {
       __nv_bfloat16* orow = a.o + (static_cast<int64_t>(b) * S + i) * a.o_row_stride +
-                            static_cast<int64_t>(h) * HD + half * 64;
+                            static_cast<int64_t>(h) * HD + half * OCOLS;
       uint4* dst = reinterpret_cast<uint4*>(orow);
 #pragma unroll
-      for (int v = 0; v < 8; ++v) {
+      for (int v = 0; v < OCOLS / 8; ++v) {
         const int x = v * 8;
         uint4 w;
         w.x = pack_bf16x2(__uint_as_float(o[x + 0]) * inv, __uint_as_float(o[x + 1]) * inv);
@@ -374,16 +399,25 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
 }  // namespace
 
-size_t fwd_smem_bytes() { return SMEM_BYTES; }
+size_t fwd_smem_bytes() { return Cfg<128>::SMEM_BYTES; }
+
+template <int HD>
+static cudaError_t launch_fwd_hd(const CUtensorMap& tq, const CUtensorMap& tk,
+                                 const CUtensorMap& tv, const FwdArgs& args, int n_blocks,
+                                 cudaStream_t st) {
+  constexpr uint32_t smem = Cfg<HD>::SMEM_BYTES;
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<HD>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  attn_fwd_kernel<HD><<<n_blocks, NUM_THREADS, smem, st>>>(tq, tk, tv, args);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_attn_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const FwdArgs& args, int n_blocks, cudaStream_t st) {
   if (n_blocks == 0) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-  if (e != cudaSuccess) return e;
-  attn_fwd_kernel<<<n_blocks, NUM_THREADS, SMEM_BYTES, st>>>(tq, tk, tv, args);
-  return cudaGetLastError();
+  if (args.dims.head_dim == 64) return launch_fwd_hd<64>(tq, tk, tv, args, n_blocks, st);
+  return launch_fwd_hd<128>(tq, tk, tv, args, n_blocks, st);
 }
 
 }  // namespace lca

@@ -45,6 +45,7 @@ struct AttnDims {
   float scale;                          // softmax scale
   float scale_log2;                     // scale * log2(e)
   int chunk;                            // work items interleaved per launch-order group
+  int head_dim;                         // 128 or 64
 };
 
 }  // namespace lca

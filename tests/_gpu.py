@@ -59,8 +59,8 @@ def to_np(t):
     return t.detach().float().cpu().numpy().astype(np.float64)
 
 
-def make_inputs(b, s, hq, hkv, seed, device="cuda"):
-    q, k, v, do = I.qkv_do(b, s, hq, hkv, 128, seed)
+def make_inputs(b, s, hq, hkv, seed, device="cuda", head_dim=128):
+    q, k, v, do = I.qkv_do(b, s, hq, hkv, head_dim, seed)
     host = [to_np(x) for x in (q, k, v, do)]
     dev = [x.to(device) for x in (q, k, v, do)]
     return host, dev

@@ -52,7 +52,9 @@ def _desc(**kw):
     ({}, (128, 96), 2),
     ({"seqlen": 0}, (128, 128), 1),
     ({"seqlen": (1 << 20) + 1}, (128, 128), 2),
-    ({"type": 12}, (128, 128), 1),
+    ({"type": 13}, (128, 128), 1),
+    ({"type": 12, "window": 0}, (128, 128), 1),         # window inside documents needs w >= 1
+    ({"type": 12, "window": 8, "num_segments": 0}, (128, 128), 1),   # ... and documents
     ({"type": -1}, (128, 128), 1),
     ({"type": 2, "window": 0}, (128, 128), 1),          # sliding window needs w >= 1
     ({"type": 7, "window": 4, "num_global": -1}, (128, 128), 1),

@@ -172,3 +172,21 @@ def test_variable_block_sparse_long_varlen():
     plan, _, grads = _run(desc, dev)
     _sampled_dq(desc, host, grads, heads=[0, 37], nrows=12, seed=7)
     _invariants(desc, host, dev, grads, plan)
+
+
+@pytest.mark.parametrize("hq,hkv,b", [(8, 2, 1), (4, 4, 1), (4, 2, 2)])
+def test_head_dim_64(hq, hkv, b):
+    """head_dim 64: every mask type (one sequence), or the batched dense masks."""
+    s = 1000
+    host, dev = make_inputs(b, s, hq, hkv, seed=640 + hq, head_dim=64)
+    descs = small_descs(s, hq, hkv, seed=7) if b == 1 else \
+        [I.make_desc(m, s, window=120) for m in (I.FULL, I.CAUSAL, I.SLIDING_WINDOW)]
+    for desc in descs:
+        _check_all(desc, host, dev, what="d64 ")
+
+
+def test_head_dim_64_medium_full_rows():
+    s = 4096
+    host, dev = make_inputs(1, s, 8, 1, seed=65, head_dim=64)
+    for mask, kw in ((I.CAUSAL, {}), (I.CAUSAL_DOCUMENT, {"doc_seed": 3})):
+        _check_all(I.make_desc(mask, s, **kw), host, dev, what="d64 ")

@@ -135,3 +135,17 @@ def test_variable_block_sparse_long_varlen_sampled():
     s = 131072
     desc = I.make_desc(I.BLOCK_SPARSE_VARIABLE, s, map_heads=8, map_seed=7, doc_seed=7)
     _sampled(desc, 1, s, 64, 8, heads=[0, 37], nrows=24, seed=99)
+
+
+@pytest.mark.parametrize("hq,hkv,b", [(8, 2, 1), (4, 4, 1), (4, 2, 2)])
+def test_head_dim_64(hq, hkv, b):
+    """head_dim 64: every mask type (one sequence), or the batched dense masks."""
+    s = 1000
+    host, dev = make_inputs(b, s, hq, hkv, seed=64 + hq, head_dim=64)
+    descs = small_descs(s, hq, hkv, seed=6) if b == 1 else \
+        [I.make_desc(m, s, window=120) for m in (I.FULL, I.CAUSAL, I.SLIDING_WINDOW)]
+    for desc in descs:
+        o, lse = _fwd(desc, dev)
+        o_ref, lse_ref = oracle.attn_fwd_ref(*host[:3], desc)
+        check_o(o, o_ref, f"d64 {desc.name}")
+        check_lse(lse, lse_ref, f"d64 {desc.name}")
