@@ -121,6 +121,11 @@ def dynamic_cases(s, map_heads, block=128, sparsity=0.5):
 
 def workload(suite, case=None):
     """(groups, description) of a named workload, or of one S:MASK dense case."""
+    groups, text = _workload(suite, case)
+    return groups, text.replace("d=128", f"d={D}")
+
+
+def _workload(suite, case=None):
     if case is not None:
         s_txt, m_txt = case.split(":")
         s = int(s_txt)
@@ -633,12 +638,19 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--suite", choices=SUITES, default="dense",
                     help="workload to time (default: the dense regular masks)")
+    ap.add_argument("--head-dim", type=int, choices=(64, 128), default=128,
+                    help="head dimension of the synthetic Q/K/V (the benchmark's configs use 128)")
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the timed oracle sample in the GPU arm")
     ap.add_argument("--case", default=None,
                     help="run a single S:MASK case of the dense workload (e.g. 16384:FULL) "
                          "for profiler captures; skips the end-to-end and CPU legs")
     args = ap.parse_args()
+    global D, FWD_PER_PAIR, BWD_PER_PAIR
+    D = args.head_dim
+    FWD_PER_PAIR, BWD_PER_PAIR = 4.0 * D, 10.0 * D
+    if args.suite == "dynamic" and D != 128:
+        ap.error("the dynamic suite's block scores are implemented for head_dim 128")
     if args.case:
         args.no_cpu_baseline = True
     rank = int(os.environ.get("RANK", "0"))
