@@ -10,10 +10,18 @@ is the one the CUDA library consumes:
   columns; tiles on the last row/column are clipped at S;
 * a tile is SKIP (0) when no in-range pair is allowed, FULL (1) when every
   in-range pair is allowed, PARTIAL (2) otherwise;
+* the tile byte of a non-skipped tile adds flags for its empty halves (no
+  allowed in-range pair): 4 = key columns [0, tile_k/2), 8 = key columns
+  [tile_k/2, tile_k), 16 = query rows [0, tile_q/2), 32 = query rows
+  [tile_q/2, tile_q).  The benchmark's sparse masks are built on a block grid
+  finer than a tile (64-token blocks against 128-token tiles), so a tile can
+  hold allowed pairs in one half only and a kernel can leave the other half out;
 * per (map head, query tile) row: the non-skipped key tiles in ascending order
-  with their classes (CSR: ``rowptr``, ``kt_idx``, ``kt_cls``);
+  with their class and key-half flags (tile byte & 15; CSR: ``rowptr``,
+  ``kt_idx``, ``kt_cls``);
 * per (map head, key tile) column: the non-skipped query tiles in ascending
-  order (``colptr``, ``qt_idx``, ``qt_cls``);
+  order with their class and query-half flags moved to bits 2-3 (``colptr``,
+  ``qt_idx``, ``qt_cls``);
 * work orders: row indices (h_m * nQt + qt) sorted by descending list length,
   ties by ascending index (``work_q``), and likewise for columns
   (``work_k``), i.e. longest-processing-time-first.
@@ -28,7 +36,8 @@ from .masks import mask_rows
 
 
 def tile_rows_ref(desc, tile_q: int, tile_k: int, h_m: int, qts: Sequence[int]) -> np.ndarray:
-    """Tile classes of the given query tiles of map head ``h_m``: uint8 [len(qts), nKt]."""
+    """Tile bytes of the given query tiles of map head ``h_m``: uint8 [len(qts), nKt]."""
+    assert tile_q % 2 == 0 and tile_k % 2 == 0, "tiles have two halves"
     s_len = desc.seqlen
     n_kt = (s_len + tile_k - 1) // tile_k
     out = np.zeros((len(qts), n_kt), np.uint8)
@@ -40,8 +49,24 @@ def tile_rows_ref(desc, tile_q: int, tile_k: int, h_m: int, qts: Sequence[int]) 
         all_m = np.concatenate([m, np.ones((len(rows), pad), bool)], axis=1)
         any_t = any_m.reshape(len(rows), n_kt, tile_k).any(axis=(0, 2))
         all_t = all_m.reshape(len(rows), n_kt, tile_k).all(axis=(0, 2))
-        out[a] = np.where(~any_t, 0, np.where(all_t, 1, 2)).astype(np.uint8)
+        cls = np.where(all_t, 1, 2)
+        # halves with an allowed pair: key columns of the tile, then query rows
+        key_h = any_m.reshape(len(rows), n_kt, 2, tile_k // 2).any(axis=(0, 3))
+        top = any_m[:tile_q // 2].reshape(-1, n_kt, tile_k).any(axis=(0, 2))
+        bottom = any_m[tile_q // 2:].reshape(-1, n_kt, tile_k).any(axis=(0, 2))
+        flags = (4 * ~key_h[:, 0] + 8 * ~key_h[:, 1] + 16 * ~top + 32 * ~bottom)
+        out[a] = np.where(any_t, cls + flags, 0).astype(np.uint8)
     return out
+
+
+def row_list_byte(tile_byte: np.ndarray) -> np.ndarray:
+    """Entry of a row list: the class and the key-half flags."""
+    return (tile_byte & 15).astype(np.uint8)
+
+
+def col_list_byte(tile_byte: np.ndarray) -> np.ndarray:
+    """Entry of a column list: the class and the query-half flags in bits 2-3."""
+    return ((tile_byte & 3) | ((tile_byte >> 2) & 12)).astype(np.uint8)
 
 
 def _lpt_order(lengths: np.ndarray) -> np.ndarray:
@@ -65,7 +90,7 @@ def tile_plan_ref(desc, tile_q: int, tile_k: int) -> Dict[str, np.ndarray]:
     rowptr[1:] = np.cumsum(row_len)
     kt_idx = np.concatenate([np.nonzero(r)[0] for r in rows]).astype(np.int32) \
         if rows.size else np.zeros(0, np.int32)
-    kt_cls = rows[rows != 0].astype(np.uint8)
+    kt_cls = row_list_byte(rows[rows != 0])
 
     cols = np.transpose(cls, (0, 2, 1)).reshape(hm_n * n_kt, n_qt)
     col_len = np.count_nonzero(cols, axis=1)
@@ -73,7 +98,7 @@ def tile_plan_ref(desc, tile_q: int, tile_k: int) -> Dict[str, np.ndarray]:
     colptr[1:] = np.cumsum(col_len)
     qt_idx = np.concatenate([np.nonzero(c)[0] for c in cols]).astype(np.int32) \
         if cols.size else np.zeros(0, np.int32)
-    qt_cls = cols[cols != 0].astype(np.uint8)
+    qt_cls = col_list_byte(cols[cols != 0])
 
     return {
         "cls": cls, "rowptr": rowptr, "kt_idx": kt_idx, "kt_cls": kt_cls,

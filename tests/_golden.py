@@ -64,9 +64,9 @@ def _desc_from(kv):
     return d
 
 
-def load_plan_case():
+def load_plan_case(name="plan_small.txt"):
     kv = {}
-    with open(os.path.join(GOLDEN, "plan_small.txt")) as f:
+    with open(os.path.join(GOLDEN, name)) as f:
         for ln in f:
             ln = ln.strip()
             if not ln or ln.startswith("#"):

@@ -7,24 +7,33 @@ from long_context_masked_gb300 import inputs as I
 from tests._golden import load_plan_case
 
 
-def test_hand_worked_plan():
-    desc, tq, tk, exp = load_plan_case()
+@pytest.mark.parametrize("name", ["plan_small.txt", "plan_halves.txt"])
+def test_hand_worked_plan(name):
+    desc, tq, tk, exp = load_plan_case(name)
     p = oracle.tile_plan_ref(desc, tq, tk)
     for key, val in exp.items():
         assert np.array_equal(p[key].astype(np.int64), val.astype(np.int64)), key
 
 
 def _tile_popcounts(m, tq, tk):
+    """Allowed pairs and in-range pairs per tile, and allowed pairs per tile half:
+    halves[..., 0:2] key columns [0, tk/2) / [tk/2, tk), [..., 2:4] query rows."""
     s = m.shape[0]
     nq, nk = -(-s // tq), -(-s // tk)
     out = np.zeros((nq, nk), np.int64)
     area = np.zeros((nq, nk), np.int64)
+    halves = np.zeros((nq, nk, 4), np.int64)
     for a in range(nq):
         for b in range(nk):
-            blk = m[a * tq:(a + 1) * tq, b * tk:(b + 1) * tk]
+            r0, c0 = a * tq, b * tk
+            blk = m[r0:r0 + tq, c0:c0 + tk]
             out[a, b] = blk.sum()
             area[a, b] = blk.size
-    return out, area
+            halves[a, b, 0] = m[r0:r0 + tq, c0:c0 + tk // 2].sum()
+            halves[a, b, 1] = m[r0:r0 + tq, c0 + tk // 2:c0 + tk].sum()
+            halves[a, b, 2] = m[r0:r0 + tq // 2, c0:c0 + tk].sum()
+            halves[a, b, 3] = m[r0 + tq // 2:r0 + tq, c0:c0 + tk].sum()
+    return out, area, halves
 
 
 @pytest.mark.parametrize("seed", range(4))
@@ -50,10 +59,14 @@ def test_plan_consistent_with_mask(seed):
         p = oracle.tile_plan_ref(d, tq, tk)
         for hm in range(d.map_heads):
             m = oracle.materialize_mask(d, hm)
-            pc, area = _tile_popcounts(m, tq, tk)
-            cls = p["cls"][hm]
+            pc, area, halves = _tile_popcounts(m, tq, tk)
+            cls = p["cls"][hm].astype(np.int64)
             assert ((cls == 0) == (pc == 0)).all()
-            assert ((cls == 1) == (pc == area)).all()
+            assert (((cls & 3) == 1) == (pc == area)).all()
+            assert ((cls & 3) != 3).all() and (cls < 64).all()
+            for bit, x in ((4, 0), (8, 1), (16, 2), (32, 3)):
+                flag = (cls & bit) != 0
+                assert (flag == ((pc > 0) & (halves[..., x] == 0))).all(), bit
             assert pc.sum() == oracle.n_valid_popcount(d, hm)
         # CSR rows, CSR columns and the class array describe the same tiles
         hmn, nq, nk = p["cls"].shape
@@ -61,11 +74,13 @@ def test_plan_consistent_with_mask(seed):
         for r in range(hmn * nq):
             a, b = p["rowptr"][r], p["rowptr"][r + 1]
             assert np.array_equal(p["kt_idx"][a:b], np.nonzero(rows[r])[0])
-            assert np.array_equal(p["kt_cls"][a:b], rows[r][rows[r] != 0])
+            assert np.array_equal(p["kt_cls"][a:b], rows[r][rows[r] != 0] & 15)
         cols = np.transpose(p["cls"], (0, 2, 1)).reshape(hmn * nk, nq)
         for c in range(hmn * nk):
             a, b = p["colptr"][c], p["colptr"][c + 1]
             assert np.array_equal(p["qt_idx"][a:b], np.nonzero(cols[c])[0])
+            nz = cols[c][cols[c] != 0]
+            assert np.array_equal(p["qt_cls"][a:b], (nz & 3) | ((nz >> 4) << 2))
         # longest first, ties by index, a permutation
         for key, ptr in (("work_q", "rowptr"), ("work_k", "colptr")):
             lens = np.diff(p[ptr])
