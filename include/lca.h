@@ -92,6 +92,25 @@ typedef enum {
   LCA_TILE_PARTIAL = 2  /* some pairs allowed, some not   */
 } lca_tile_class;
 
+/* Tile byte: the class in bits 0-1 and, for a non-skipped tile, one flag per half of
+ * the tile that holds no allowed in-range pair.  The benchmark's sparse masks keep
+ * blocks of a grid finer than a 128 x 128 tile (64-token blocks; summary page,
+ * appendix A.2 "Block Partitioning"), which leaves tiles with pairs in one half only;
+ * the kernels leave an empty half out.  A skipped tile's byte is 0.
+ *   cls     the whole tile byte (bits 0-5);
+ *   kt_cls  row-list entry: the class and the key-half flags (tile byte & 15);
+ *   qt_cls  column-list entry: the class and the query-half flags moved down to
+ *           bits 2-3 ((byte & 3) | ((byte >> 4) << 2)).
+ * In either list, bits 2-3 are the flags of the halves the list's kernel iterates
+ * against: (entry >> 2) & 1 for the first half, (entry >> 3) & 1 for the second. */
+enum {
+  LCA_TILE_CLASS_MASK = 3,
+  LCA_TILE_KEY_HALF0_EMPTY = 4,     /* key columns [0, tile_k / 2)      */
+  LCA_TILE_KEY_HALF1_EMPTY = 8,     /* key columns [tile_k / 2, tile_k) */
+  LCA_TILE_QUERY_HALF0_EMPTY = 16,  /* query rows [0, tile_q / 2)       */
+  LCA_TILE_QUERY_HALF1_EMPTY = 32   /* query rows [tile_q / 2, tile_q)  */
+};
+
 /* Mask descriptor ("unified data format" of the benchmark: summary page, section 2.2;
  * reading note, "Key design" 2).  Fields a type does not use are ignored.
  * Device arrays are read during lca_mask_build only (the plan keeps its own copies). */
@@ -153,7 +172,8 @@ lca_status lca_mask_build(const lca_mask_desc* desc, int tile_q, int tile_k, voi
 lca_status lca_plan_get_info(const lca_plan* plan, lca_plan_info* info);
 
 /* Copy a plan's arrays to HOST buffers (any pointer may be NULL to skip it), sizes
- * from lca_plan_info: cls [map_heads*n_qt*n_kt] uint8; rowptr [map_heads*n_qt+1],
+ * from lca_plan_info: cls [map_heads*n_qt*n_kt] uint8 tile bytes (class and empty-half
+ * flags, see LCA_TILE_CLASS_MASK); rowptr [map_heads*n_qt+1],
  * kt_idx [nnz], kt_cls [nnz] (per (h_m, qt) row, ascending kt); colptr
  * [map_heads*n_kt+1], qt_idx [nnz], qt_cls [nnz] (per (h_m, kt) column, ascending qt);
  * work_q [map_heads*n_qt], work_k [map_heads*n_kt] (row/column indices h_m*n + t,

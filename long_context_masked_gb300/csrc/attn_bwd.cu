@@ -19,8 +19,14 @@
 //               the dP and dQ MMAs from there.
 // Warp roles as in the forward: warps 8 and 10 issue TMA loads, warp 9 owns TMEM and
 // issues the MMAs, warps 0-7 (two threads per TMEM lane, 64 columns each) turn S/dP
-// into P/dS.  All waits are bounded.
+// into P/dS.  Where a CTA walks at least 64 plan entries and at least half of them flag
+// one half of their tile as empty (query rows for dK/dV, key columns for dQ), such a
+// tile runs at half width: N = 64 recompute MMAs, half the k-steps of the accumulating MMAs, and the
+// softmax warps of that half stay idle.
+// All waits are bounded.
 #include <cuda_runtime.h>
+
+#include <type_traits>
 
 #include "attn_kernels.h"
 #include "lca_device.cuh"
@@ -32,7 +38,9 @@ namespace {
 constexpr int BM = 128;
 constexpr int BN = 128;
 constexpr uint32_t HALF = BM * 64 * 2;   // one 128-byte-swizzled 64-column half, 16 KB
+constexpr uint64_t ROWS64_STEP = (64 * 128) >> 4;   // descriptor step to row 64 of a half
 constexpr float LOG2E = 1.4426950408889634f;
+constexpr int HALF_SHARE = 2;   // half-width path: half of a list's entries flagged
 
 // ------------------------------------------------------------------ preprocess
 
@@ -240,6 +248,22 @@ struct ColWalk {
   }
 };
 
+// use_half_path over the column lists a dK/dV CTA walks.  Warp-wide.
+__device__ __forceinline__ bool walk_use_half_path(const PlanDev& pl, int kt, int hk,
+                                                   const AttnDims& d, int lane) {
+  int f = 0, n = 0;
+  int prev = -1;
+  for (int gi = 0; gi < d.group; ++gi) {
+    const int col = ((hk * d.group + gi) / d.heads_per_map) * pl.n_kt + kt;
+    if (col == prev) continue;   // query heads sharing a map share its list
+    prev = col;
+    const int p0 = __ldg(pl.colptr + col), p1 = __ldg(pl.colptr + col + 1);
+    n += p1 - p0;
+    for (int x = p0 + lane; x < p1; x += 32) f += (__ldg(pl.qt_cls + x) & 12) != 0;
+  }
+  return half_path(__reduce_add_sync(0xFFFFFFFFu, f), n, HALF_SHARE);
+}
+
 template <int HD_>
 __global__ void __launch_bounds__(KV_THREADS, 1)
 bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -376,8 +400,10 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       }
     }
   } else if (warp == WARP_MMA) {
+    const bool halves = walk_use_half_path(pl, kt, hk, dm, lane);
     if (lane == 0) {
       constexpr uint32_t IDESC_SS = idesc_bf16(BN, BM, 0, 0);  // S^T, dP^T
+      constexpr uint32_t IDESC_SS_HALF = idesc_bf16(BN, BM / 2, 0, 0);
       constexpr uint32_t IDESC_TS = idesc_bf16(BN, HD, 0, 1);  // dV, dK (B MN-major)
       const uint64_t dk_ = desc_kmajor(base_u32 + KV_OFF_K, 0, HALF);
       const uint64_t dv_ = desc_kmajor(base_u32 + KV_OFF_V, 0, HALF);
@@ -391,67 +417,109 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         int h, qt, cls;
         while (w2.next(h, qt, cls)) ++total;
       }
-      auto issue_s = [&](int t) {
-        const uint64_t dq = dq_k0 + (t % KV_QST) * stage_step(TILE);
-        tc_fence_after();
+      // A step whose entry flags a query half as empty recomputes S^T / dP^T for the
+      // other half only (N = 64 on its 64 Q / dO rows, into its 64 columns) and gives
+      // dV / dK only that half's k-steps.
+      auto recompute = [&](uint32_t tcol, uint64_t da, uint64_t db, int empty) {
+        uint32_t idesc = IDESC_SS;
+        if (empty != 0) {
+          const int hf = empty == 1 ? 1 : 0;
+          idesc = IDESC_SS_HALF;
+          tcol += hf * 64;
+          db += hf * ROWS64_STEP;
+        }
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk)
-          umma_bf16_ss(tmem + KV_TM_S, dk_ + kmajor_step(kk, HALF), dq + kmajor_step(kk, HALF),
-                       IDESC_SS, kk > 0 ? 1u : 0u);
+          umma_bf16_ss(tmem + tcol, da + kmajor_step(kk, HALF), db + kmajor_step(kk, HALF), idesc,
+                       kk > 0 ? 1u : 0u);
+      };
+      auto accumulate = [&](uint32_t dcol, uint32_t acol, uint64_t db, int empty, bool first) {
+        if (empty == 0) {
+#pragma unroll
+          for (int kk = 0; kk < BM / 16; ++kk)
+            umma_bf16_ts(tmem + dcol, tmem + acol + kv_pair_col(kk), db + mnmajor_step(kk),
+                         IDESC_TS, (!first || kk > 0) ? 1u : 0u);
+        } else {
+          // the four k-steps of the other query half only
+          const int k0 = empty == 1 ? 4 : 0;
+          const uint32_t a0 = tmem + acol + kv_pair_col(k0);
+          const uint64_t b0 = db + mnmajor_step(k0);
+#pragma unroll
+          for (int kk = 0; kk < BM / 32; ++kk)
+            umma_bf16_ts(tmem + dcol, a0 + kk * 8, b0 + mnmajor_step(kk), IDESC_TS,
+                         (!first || kk > 0) ? 1u : 0u);
+        }
+      };
+      auto issue_s = [&](int t, int empty) {
+        tc_fence_after();
+        recompute(KV_TM_S, dk_, dq_k0 + (t % KV_QST) * stage_step(TILE), empty);
         umma_commit(&bar.s_full);
       };
-      auto issue_dp = [&](int t) {
-        const uint64_t ddo = ddo_k0 + (t % KV_DOST) * stage_step(TILE);
+      auto issue_dp = [&](int t, int empty) {
         tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk)
-          umma_bf16_ss(tmem + KV_TM_DP, dv_ + kmajor_step(kk, HALF), ddo + kmajor_step(kk, HALF),
-                       IDESC_SS, kk > 0 ? 1u : 0u);
+        recompute(KV_TM_DP, dv_, ddo_k0 + (t % KV_DOST) * stage_step(TILE), empty);
         umma_commit(&bar.dp_full);
       };
-      auto issue_dv = [&](int t) {
-        const uint64_t ddo = ddo_m0 + (t % KV_DOST) * stage_step(TILE);
+      auto issue_dv = [&](int t, int empty) {
         tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < BM / 16; ++kk)
-          umma_bf16_ts(tmem + KV_TM_DV, tmem + KV_TM_S + kv_pair_col(kk), ddo + mnmajor_step(kk),
-                       IDESC_TS, (t > 0 || kk > 0) ? 1u : 0u);
+        accumulate(KV_TM_DV, KV_TM_S, ddo_m0 + (t % KV_DOST) * stage_step(TILE), empty, t == 0);
         umma_commit(&bar.dv_done);
       };
-      auto issue_dk = [&](int t) {
+      auto issue_dk = [&](int t, int empty) {
         const int st = t % KV_QST;
-        const uint64_t dq = dq_m0 + st * stage_step(TILE);
         tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < BM / 16; ++kk)
-          umma_bf16_ts(tmem + KV_TM_DK, tmem + KV_TM_DP + kv_pair_col(kk), dq + mnmajor_step(kk),
-                       IDESC_TS, (t > 0 || kk > 0) ? 1u : 0u);
+        accumulate(KV_TM_DK, KV_TM_DP, dq_m0 + st * stage_step(TILE), empty, t == 0);
         umma_commit(&bar.dk_done);
         umma_commit(&bar.q_empty[st]);
         umma_commit(&bar.do_empty[t % KV_DOST]);   // D(t) is read until ds_ready(t)
       };
-      mbar_wait(&bar.kv_full, 0, wc);
-      if (total > 0) {
-        mbar_wait(&bar.q_full[0], 0, wc);
-        issue_s(0);
-        mbar_wait(&bar.do_full[0], 0, wc);
-        issue_dp(0);
-      }
-      for (int t = 0; t < total && !bar.abort; ++t) {
-        mbar_wait(&bar.p_ready, t & 1, wc);
-        issue_dv(t);
-        mbar_wait(&bar.ds_ready, t & 1, wc);
-        issue_dk(t);
-        const int n = t + 1;
-        if (n < total) {
-          mbar_wait(&bar.q_full[n % KV_QST], (n / KV_QST) & 1, wc);
-          mbar_wait(&bar.dv_done, t & 1, wc);      // P^T(t) consumed
-          issue_s(n);
-          mbar_wait(&bar.do_full[n % KV_DOST], (n / KV_DOST) & 1, wc);
-          mbar_wait(&bar.dk_done, t & 1, wc);      // dS^T(t) consumed
-          issue_dp(n);
+      // Key tiles that walk_use_half_path turns down run the loop without any flag
+      // handling (a separate instantiation; the issue loop is sensitive to extra work).
+      // In the flag-aware loop the steps' entries come from the issuer's own walk, one
+      // step ahead of use: a load consumed right away holds the issue of the next MMAs
+      // back.
+      auto run = [&](auto halves_c) {
+        constexpr bool HALVES = decltype(halves_c)::value;
+        ColWalk iw = walk;
+        int e_next = 0;
+        auto fetch = [&]() {
+          int h, qt, cls;
+          if (iw.next(h, qt, cls)) e_next = cls;
+        };
+        int eh = 0;          // empty halves of step t
+        mbar_wait(&bar.kv_full, 0, wc);
+        if (total > 0) {
+          if constexpr (HALVES) {
+            fetch();
+            eh = entry_empty_halves(e_next);
+            fetch();
+          }
+          mbar_wait(&bar.q_full[0], 0, wc);
+          issue_s(0, eh);
+          mbar_wait(&bar.do_full[0], 0, wc);
+          issue_dp(0, eh);
         }
-      }
+        for (int t = 0; t < total && !bar.abort; ++t) {
+          mbar_wait(&bar.p_ready, t & 1, wc);
+          issue_dv(t, eh);
+          mbar_wait(&bar.ds_ready, t & 1, wc);
+          issue_dk(t, eh);
+          const int n = t + 1;
+          if (n < total) {
+            if constexpr (HALVES) {
+              eh = entry_empty_halves(e_next);
+              fetch();
+            }
+            mbar_wait(&bar.q_full[n % KV_QST], (n / KV_QST) & 1, wc);
+            mbar_wait(&bar.dv_done, t & 1, wc);      // P^T(t) consumed
+            issue_s(n, eh);
+            mbar_wait(&bar.do_full[n % KV_DOST], (n / KV_DOST) & 1, wc);
+            mbar_wait(&bar.dk_done, t & 1, wc);      // dS^T(t) consumed
+            issue_dp(n, eh);
+          }
+        }
+      };
+      if (halves) run(std::true_type{}); else run(std::false_type{});
     }
   } else {
     // ------------------------------------------------ softmax warps 0-7
@@ -463,67 +531,88 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const float sl2 = dm.scale_log2;
     const RowSpan cs = col_span(a.mask, min(j, S - 1));
     MapCursor mcur;
-    int h, qt, cls, t = 0;
-    while (walk.next(h, qt, cls)) {
-      const bool masked = cls != LCA_TILE_FULL || kt * BN + BN > S || qt * BM + BM > S;
-      uint32_t bits[2] = {0u, 0u};
-      if (masked && jvalid)
-        col_tile_bits<2>(a.mask, h / dm.heads_per_map, j, qt * BM + half * 64, cs, bits, &mcur);
-      const float* lse2 =
-          reinterpret_cast<const float*>(base + KV_OFF_LSE + (t % KV_QST) * ROWV) + half * 64;
-      const float* dsum =
-          reinterpret_cast<const float*>(base + KV_OFF_D + (t % KV_DOST) * ROWV) + half * 64;
+    int t = 0;
+    // Key tiles that walk_use_half_path turns down run the loop without the idle check
+    // (a separate instantiation).
+    auto steps = [&](auto halves_c) {
+      constexpr bool HALVES = decltype(halves_c)::value;
+      int h, qt, cls;
+      while (walk.next(h, qt, cls)) {
+        // this warp's query half holds no pair of the tile: nothing to read or write
+        const bool idle = HALVES && ((entry_empty_halves(cls) >> half) & 1);
+        const bool masked =
+            entry_class(cls) != LCA_TILE_FULL || kt * BN + BN > S || qt * BM + BM > S;
+        uint32_t bits[2] = {0u, 0u};
+        if (masked && jvalid && !idle)
+          col_tile_bits<2>(a.mask, h / dm.heads_per_map, j, qt * BM + half * 64, cs, bits, &mcur);
+        const float* lse2 =
+            reinterpret_cast<const float*>(base + KV_OFF_LSE + (t % KV_QST) * ROWV) + half * 64;
+        const float* dsum =
+            reinterpret_cast<const float*>(base + KV_OFF_D + (t % KV_DOST) * ROWV) + half * 64;
 
-      // The LSE2 / D rows were written by bulk copies that complete on q_full / do_full;
-      // observing those phases here (already complete: the stages are refilled only
-      // after this step's ds_ready) makes the rows visible to this thread.
-      mbar_wait(&bar.s_full, t & 1, wc);
-      mbar_wait(&bar.q_full[t % KV_QST], (t / KV_QST) & 1, wc);
-      __syncwarp();
-      tc_fence_after();
-      uint32_t r[64];
-      tmem_ld64(lane_addr + KV_TM_S, r);
-      float p[64];
+        // The LSE2 / D rows were written by bulk copies that complete on q_full / do_full;
+        // observing those phases here (already complete: the stages are refilled only
+        // after this step's ds_ready) makes the rows visible to this thread.
+        mbar_wait(&bar.s_full, t & 1, wc);
+        mbar_wait(&bar.q_full[t % KV_QST], (t / KV_QST) & 1, wc);
+        __syncwarp();
+        tc_fence_after();
+        if (idle) {
+          tc_fence_before();
+          mbar_arrive(&bar.p_ready);
+          mbar_wait(&bar.dp_full, t & 1, wc);
+          mbar_wait(&bar.do_full[t % KV_DOST], (t / KV_DOST) & 1, wc);
+          tc_fence_before();
+          mbar_arrive(&bar.ds_ready);
+          ++t;
+          continue;
+        }
+        uint32_t r[64];
+        tmem_ld64(lane_addr + KV_TM_S, r);
+        float p[64];
 #pragma unroll
-      for (int x = 0; x < 64; x += 4) {
-        const float4 l = *reinterpret_cast<const float4*>(lse2 + x);
-        p[x + 0] = ex2_approx(fmaf(__uint_as_float(r[x + 0]), sl2, -l.x));
-        p[x + 1] = ex2_approx(fmaf(__uint_as_float(r[x + 1]), sl2, -l.y));
-        p[x + 2] = ex2_approx(fmaf(__uint_as_float(r[x + 2]), sl2, -l.z));
-        p[x + 3] = ex2_approx(fmaf(__uint_as_float(r[x + 3]), sl2, -l.w));
-      }
-      if (masked) {
+        for (int x = 0; x < 64; x += 4) {
+          const float4 l = *reinterpret_cast<const float4*>(lse2 + x);
+          p[x + 0] = ex2_approx(fmaf(__uint_as_float(r[x + 0]), sl2, -l.x));
+          p[x + 1] = ex2_approx(fmaf(__uint_as_float(r[x + 1]), sl2, -l.y));
+          p[x + 2] = ex2_approx(fmaf(__uint_as_float(r[x + 2]), sl2, -l.z));
+          p[x + 3] = ex2_approx(fmaf(__uint_as_float(r[x + 3]), sl2, -l.w));
+        }
+        if (masked) {
 #pragma unroll
-        for (int x = 0; x < 64; ++x)
-          if (!((bits[x >> 5] >> (x & 31)) & 1u)) p[x] = 0.f;
-      }
-      uint32_t pk[32];
+          for (int x = 0; x < 64; ++x)
+            if (!((bits[x >> 5] >> (x & 31)) & 1u)) p[x] = 0.f;
+        }
+        uint32_t pk[32];
 #pragma unroll
-      for (int x = 0; x < 32; ++x) pk[x] = pack_bf16x2(p[2 * x], p[2 * x + 1]);
-      tmem_st32(lane_addr + KV_TM_S, pk);
-      tc_fence_before();
-      mbar_arrive(&bar.p_ready);
+        for (int x = 0; x < 32; ++x) pk[x] = pack_bf16x2(p[2 * x], p[2 * x + 1]);
+        tmem_st32(lane_addr + KV_TM_S, pk);
+        tc_fence_before();
+        mbar_arrive(&bar.p_ready);
 
-      mbar_wait(&bar.dp_full, t & 1, wc);
-      mbar_wait(&bar.do_full[t % KV_DOST], (t / KV_DOST) & 1, wc);
-      __syncwarp();
-      tc_fence_after();
-      tmem_ld64(lane_addr + KV_TM_DP, r);
+        mbar_wait(&bar.dp_full, t & 1, wc);
+        mbar_wait(&bar.do_full[t % KV_DOST], (t / KV_DOST) & 1, wc);
+        __syncwarp();
+        tc_fence_after();
+        tmem_ld64(lane_addr + KV_TM_DP, r);
 #pragma unroll
-      for (int x = 0; x < 64; x += 4) {
-        const float4 dd = *reinterpret_cast<const float4*>(dsum + x);
-        p[x + 0] *= __uint_as_float(r[x + 0]) - dd.x;
-        p[x + 1] *= __uint_as_float(r[x + 1]) - dd.y;
-        p[x + 2] *= __uint_as_float(r[x + 2]) - dd.z;
-        p[x + 3] *= __uint_as_float(r[x + 3]) - dd.w;
+        for (int x = 0; x < 64; x += 4) {
+          const float4 dd = *reinterpret_cast<const float4*>(dsum + x);
+          p[x + 0] *= __uint_as_float(r[x + 0]) - dd.x;
+          p[x + 1] *= __uint_as_float(r[x + 1]) - dd.y;
+          p[x + 2] *= __uint_as_float(r[x + 2]) - dd.z;
+          p[x + 3] *= __uint_as_float(r[x + 3]) - dd.w;
+        }
+#pragma unroll
+        for (int x = 0; x < 32; ++x) pk[x] = pack_bf16x2(p[2 * x], p[2 * x + 1]);
+        tmem_st32(lane_addr + KV_TM_DP, pk);
+        tc_fence_before();
+        mbar_arrive(&bar.ds_ready);
+        ++t;
       }
-#pragma unroll
-      for (int x = 0; x < 32; ++x) pk[x] = pack_bf16x2(p[2 * x], p[2 * x + 1]);
-      tmem_st32(lane_addr + KV_TM_DP, pk);
-      tc_fence_before();
-      mbar_arrive(&bar.ds_ready);
-      ++t;
-    }
+    };
+    if (walk_use_half_path(pl, kt, hk, dm, lane)) steps(std::true_type{});
+    else steps(std::false_type{});
     if (t > 0) {
       mbar_wait(&bar.dv_done, (t - 1) & 1, wc);
       mbar_wait(&bar.dk_done, (t - 1) & 1, wc);
@@ -572,6 +661,7 @@ struct DqBars {
   uint32_t tmem_base;
   int abort;
 };
+static_assert(sizeof(DqBars) <= 256, "barrier block overflows its shared-memory slot");
 
 template <int HD_>
 __global__ void __launch_bounds__(DQ_THREADS, 1)
@@ -686,8 +776,10 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       }
     }
   } else if (warp == WARP_MMA) {
+    const bool halves = use_half_path(pl.kt_cls + beg, n_tiles, HALF_SHARE, lane);
     if (lane == 0) {
       constexpr uint32_t IDESC_NT = idesc_bf16(BM, BN, 0, 0);  // S, dP
+      constexpr uint32_t IDESC_NT_HALF = idesc_bf16(BM, BN / 2, 0, 0);
       constexpr uint32_t IDESC_NN = idesc_bf16(BM, HD, 0, 1);  // dQ (B = K MN-major)
       const uint64_t dq_ = desc_kmajor(base_u32 + DQ_OFF_Q, 0, HALF);
       const uint64_t dk_k0 = desc_kmajor(base_u32 + DQ_OFF_K, 0, HALF);
@@ -699,56 +791,94 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       // dS(n+1) only after dQ(n) completed, so ds_ready is at most one phase ahead.
       // dP first: its commit releases the V stage half a group earlier, and S (the last
       // reader of K until dQ) gets its K tile later.
-      auto issue_sdp = [&](int n) {
-        const uint64_t dk = dk_k0 + (n % DQ_KST) * stage_step(TILE);
-        const uint64_t dv = dv_k0 + (n % DQ_VST) * stage_step(TILE);
+      auto issue_sdp = [&](int n, int empty) {
+        uint64_t dk = dk_k0 + (n % DQ_KST) * stage_step(TILE);
+        uint64_t dv = dv_k0 + (n % DQ_VST) * stage_step(TILE);
+        uint32_t idesc = IDESC_NT, col = 0;
+        if (empty != 0) {   // one key half only: its 64 K / V rows into its 64 columns
+          const int hf = empty == 1 ? 1 : 0;
+          idesc = IDESC_NT_HALF;
+          col = hf * 64;
+          dk += hf * ROWS64_STEP;
+          dv += hf * ROWS64_STEP;
+        }
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk)
-          umma_bf16_ts(tmem + DQ_TM_DP, tmem + DQ_TM_DO + kk * 8, dv + kmajor_step(kk, HALF),
-                       IDESC_NT, kk > 0 ? 1u : 0u);
+          umma_bf16_ts(tmem + DQ_TM_DP + col, tmem + DQ_TM_DO + kk * 8,
+                       dv + kmajor_step(kk, HALF), idesc, kk > 0 ? 1u : 0u);
         umma_commit(&bar.v_empty[n % DQ_VST]);
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk)
-          umma_bf16_ss(tmem + DQ_TM_S, dq_ + kmajor_step(kk, HALF), dk + kmajor_step(kk, HALF),
-                       IDESC_NT, kk > 0 ? 1u : 0u);
+          umma_bf16_ss(tmem + DQ_TM_S + col, dq_ + kmajor_step(kk, HALF),
+                       dk + kmajor_step(kk, HALF), idesc, kk > 0 ? 1u : 0u);
         umma_commit(&bar.sdp_full);
       };
-      auto issue_dq = [&](int n) {
+      auto issue_dq = [&](int n, int empty) {
         const uint64_t dk = dk_m0 + (n % DQ_KST) * stage_step(TILE);
         tc_fence_after();
+        if (empty == 0) {
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-          umma_bf16_ts(tmem + DQ_TM_DQ, tmem + DQ_TM_DS + kk * 8, dk + mnmajor_step(kk),
-                       IDESC_NN, (n > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < BN / 16; ++kk)
+            umma_bf16_ts(tmem + DQ_TM_DQ, tmem + DQ_TM_DS + kk * 8, dk + mnmajor_step(kk),
+                         IDESC_NN, (n > 0 || kk > 0) ? 1u : 0u);
+        } else {
+          // the four k-steps of the other key half only
+          const int k0 = empty == 1 ? 4 : 0;
+#pragma unroll
+          for (int kk = 0; kk < BN / 32; ++kk)
+            umma_bf16_ts(tmem + DQ_TM_DQ, tmem + DQ_TM_DS + (k0 + kk) * 8,
+                         dk + mnmajor_step(k0 + kk), IDESC_NN, (n > 0 || kk > 0) ? 1u : 0u);
+        }
         umma_commit(&bar.dq_done);
         umma_commit(&bar.k_empty[n % DQ_KST]);
       };
-      mbar_wait(&bar.q_full, 0, wc);
-      mbar_wait(&bar.do_ready, 0, wc);
-      int n_sdp = 0, n_dq = 0;
-      uint64_t idle_since = 0;
-      while (n_dq < n_tiles && !bar.abort) {
-        bool progress = false;
-        if (n_sdp < n_tiles && (n_sdp == 0 || mbar_test(&bar.sdp_free, (n_sdp - 1) & 1)) &&
-            mbar_test(&bar.k_full[n_sdp % DQ_KST], (n_sdp / DQ_KST) & 1) &&
-            mbar_test(&bar.v_full[n_sdp % DQ_VST], (n_sdp / DQ_VST) & 1)) {
-          issue_sdp(n_sdp++);
-          progress = true;
+      // Rows that use_half_path turns down run the loop without any flag handling (a
+      // separate instantiation; the issue loop is sensitive to extra work).  In the
+      // flag-aware loop the entry of tile n_sdp is loaded one SdP issue ahead of use (a
+      // load consumed right away holds the issue of the next MMAs back), then kept for
+      // dQ in a register ring, two bits at (n % 16) (the two counters stay a few tiles
+      // apart).
+      auto run = [&](auto halves_c) {
+        constexpr bool HALVES = decltype(halves_c)::value;
+        mbar_wait(&bar.q_full, 0, wc);
+        mbar_wait(&bar.do_ready, 0, wc);
+        int n_sdp = 0, n_dq = 0;
+        int e_sdp = (HALVES && n_tiles > 0) ? __ldg(pl.kt_cls + tile(0)) : 0;
+        uint32_t ring = 0u;
+        uint64_t idle_since = 0;
+        while (n_dq < n_tiles && !bar.abort) {
+          bool progress = false;
+          if (n_sdp < n_tiles && (n_sdp == 0 || mbar_test(&bar.sdp_free, (n_sdp - 1) & 1)) &&
+              mbar_test(&bar.k_full[n_sdp % DQ_KST], (n_sdp / DQ_KST) & 1) &&
+              mbar_test(&bar.v_full[n_sdp % DQ_VST], (n_sdp / DQ_VST) & 1)) {
+            if constexpr (HALVES) {
+              const int empty = entry_empty_halves(e_sdp);
+              const int sh = 2 * (n_sdp % 16);
+              ring = (ring & ~(3u << sh)) | (static_cast<uint32_t>(empty) << sh);
+              issue_sdp(n_sdp++, empty);
+              if (n_sdp < n_tiles) e_sdp = __ldg(pl.kt_cls + tile(n_sdp));
+            } else {
+              issue_sdp(n_sdp++, 0);
+            }
+            progress = true;
+          }
+          if (n_dq < n_sdp && mbar_test(&bar.ds_ready, n_dq & 1)) {
+            issue_dq(n_dq, HALVES ? static_cast<int>((ring >> (2 * (n_dq % 16))) & 3) : 0);
+            ++n_dq;
+            progress = true;
+          }
+          if (progress) {
+            idle_since = 0;
+          } else if (idle_since == 0) {
+            idle_since = globaltimer_ns();
+          } else if (globaltimer_ns() - idle_since > a.timeout_ns) {
+            bar.abort = 1;
+            atomicOr(a.err, LCA_DEVERR_TIMEOUT);
+          }
         }
-        if (n_dq < n_sdp && mbar_test(&bar.ds_ready, n_dq & 1)) {
-          issue_dq(n_dq++);
-          progress = true;
-        }
-        if (progress) {
-          idle_since = 0;
-        } else if (idle_since == 0) {
-          idle_since = globaltimer_ns();
-        } else if (globaltimer_ns() - idle_since > a.timeout_ns) {
-          bar.abort = 1;
-          atomicOr(a.err, LCA_DEVERR_TIMEOUT);
-        }
-      }
+      };
+      if (halves) run(std::true_type{}); else run(std::false_type{});
     }
   } else {
     const int quarter = warp & 3, half = warp >> 2;
@@ -785,27 +915,48 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     }
     const RowSpan sp = row_span(a.mask, min(i, S - 1));
     MapCursor mcur;
-    for (int n = 0; n < n_tiles; ++n) {
-      const int kt = __ldg(pl.kt_idx + tile(n));
-      const int cls = __ldg(pl.kt_cls + tile(n));
-      const bool masked = cls != LCA_TILE_FULL || kt * BN + BN > S || qt * BM + BM > S;
-      uint32_t bits[2] = {0u, 0u};
-      if (masked && valid) row_tile_bits<2>(a.mask, hm, i, kt * BN + half * 64, sp, bits, &mcur);
-      mbar_wait(&bar.sdp_full, n & 1, wc);
-      __syncwarp();
-      tc_fence_after();
-      uint32_t sr[64], dr[64];
-      tmem_ld64x2(lane_addr + DQ_TM_S, lane_addr + DQ_TM_DP, sr, dr);
-      tc_fence_before();
-      mbar_arrive(&bar.sdp_free);
-      uint32_t dk[32];
-      ds_half(sr, dr, masked, bits, sl2, lse2, dsum, dk);
-      if (n >= 1) mbar_wait(&bar.dq_done, (n - 1) & 1, wc);   // dQ_{n-1} read dS_{n-1}
-      __syncwarp();
-      tc_fence_after();
-      tmem_st32(quarter_addr + DQ_TM_DS + half * 32, dk);
+    // One key tile; IDLE: this warp's key half holds no pair of the tile (nothing to read
+    // or write, only the barrier protocol).  Two instantiations keep the common path's
+    // code exactly that of a full-width tile.
+    auto tile_step = [&](int n, auto idle_c) {
+      constexpr bool IDLE = decltype(idle_c)::value;
+      if constexpr (!IDLE) {
+        const int kt = __ldg(pl.kt_idx + tile(n));
+        const int e = __ldg(pl.kt_cls + tile(n));
+        const bool masked =
+            entry_class(e) != LCA_TILE_FULL || kt * BN + BN > S || qt * BM + BM > S;
+        uint32_t bits[2] = {0u, 0u};
+        if (masked && valid) row_tile_bits<2>(a.mask, hm, i, kt * BN + half * 64, sp, bits, &mcur);
+        mbar_wait(&bar.sdp_full, n & 1, wc);
+        __syncwarp();
+        tc_fence_after();
+        uint32_t sr[64], dr[64];
+        tmem_ld64x2(lane_addr + DQ_TM_S, lane_addr + DQ_TM_DP, sr, dr);
+        tc_fence_before();
+        mbar_arrive(&bar.sdp_free);
+        uint32_t dk[32];
+        ds_half(sr, dr, masked, bits, sl2, lse2, dsum, dk);
+        if (n >= 1) mbar_wait(&bar.dq_done, (n - 1) & 1, wc);   // dQ_{n-1} read dS_{n-1}
+        __syncwarp();
+        tc_fence_after();
+        tmem_st32(quarter_addr + DQ_TM_DS + half * 32, dk);
+      } else {
+        mbar_wait(&bar.sdp_full, n & 1, wc);
+        mbar_arrive(&bar.sdp_free);
+        if (n >= 1) mbar_wait(&bar.dq_done, (n - 1) & 1, wc);
+      }
       tc_fence_before();
       mbar_arrive(&bar.ds_ready);
+    };
+    if (!use_half_path(pl.kt_cls + beg, n_tiles, HALF_SHARE, lane)) {
+      for (int n = 0; n < n_tiles; ++n) tile_step(n, std::false_type{});
+    } else {
+      for (int n = 0; n < n_tiles; ++n) {
+        if ((entry_empty_halves(__ldg(pl.kt_cls + tile(n))) >> half) & 1)
+          tile_step(n, std::true_type{});
+        else
+          tile_step(n, std::false_type{});
+      }
     }
     if (n_tiles > 0) {
       mbar_wait(&bar.dq_done, (n_tiles - 1) & 1, wc);

@@ -19,10 +19,17 @@
 //               (bf16 pairs) back into the TMEM columns of S_n for the PV MMA, rescale
 //               the O accumulator in TMEM when the running max moves by more than 2^8
 //               (exact after the final 1/l normalisation), then the epilogue.
+// In a row of at least 64 plan entries of which at least a quarter flag one key half of
+// their tile as empty (no allowed pair: block maps on a grid finer than the tile, ragged tails),
+// such a tile runs at half width: S is an N = 64 MMA on the other half's keys, PV takes
+// only that half's k-steps, and the softmax warps of the empty half only join the
+// row-max exchange.  Other rows run loops without any flag handling.
 // Keeping P in TMEM matters on this part: an M = N = 128 MMA with both operands in
 // shared memory reads 128 B/clk, the whole shared-memory bandwidth of the SM.
 // Tile = 128 x 128, head_dim 128 or 64.  All waits are bounded.
 #include <cuda_runtime.h>
+
+#include <type_traits>
 
 #include "attn_kernels.h"
 #include "lca_device.cuh"
@@ -34,7 +41,9 @@ namespace {
 constexpr int BM = 128;              // query rows per tile
 constexpr int BN = 128;              // keys per tile
 constexpr uint32_t HALF_BYTES = BM * 64 * 2;   // one 128-byte-swizzled 64-column half, 16 KB
+constexpr uint64_t ROWS64_STEP = (64 * 128) >> 4;   // descriptor step to row 64 of a half
 constexpr float RESCALE_THRESHOLD = 8.0f;      // log2 units
+constexpr int HALF_SHARE = 4;   // half-width path: a quarter of a row's entries flagged
 
 constexpr int NUM_THREADS = 352;     // 8 softmax warps, MMA issuer, K and V producers
 constexpr int SOFTMAX_THREADS = 256;
@@ -86,6 +95,7 @@ struct Bars {
   uint32_t tmem_base;
   int abort;
 };
+static_assert(sizeof(Bars) <= 256, "barrier block overflows its shared-memory slot");
 
 __device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, int kk) {
   return desc_kmajor(tile, kk, HALF_BYTES);
@@ -211,8 +221,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
   } else if (warp == WARP_MMA) {
     // ------------------------------------------------ MMA issuer
+    // Rows that use_half_path turns down (every dense mask) run the plain loop; the
+    // flag-aware loop is a separate instantiation, so the plain one carries no per-tile
+    // flag handling (the issue loop is sensitive to any extra work).
+    const bool halves = use_half_path(pl.kt_cls + beg, n_tiles, HALF_SHARE, lane);
     if (lane == 0) {
       constexpr uint32_t IDESC_QK = idesc_bf16(BM, BN, 0, 0);
+      constexpr uint32_t IDESC_QK_HALF = idesc_bf16(BM, BN / 2, 0, 0);
       constexpr uint32_t IDESC_PV = idesc_bf16(BM, HD, 0, 1);
       const uint64_t dq0 = kmajor_desc(base_u32 + OFF_Q, 0);
       const uint64_t dk0 = kmajor_desc(base_u32 + OFF_K, 0);
@@ -221,7 +236,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       // reuses that buffer; it is issued after PV_j and tcgen05 MMAs of one thread run
       // in issue order, so PV_j has read P_j before S_{j+3} overwrites it (and PV_j
       // waited for the softmax of tile j, so S_j was consumed).
-      auto issue_pv = [&](int j) {
+      auto issue_pv = [&](int j, int empty) {
         const int sb = j % NSB;
         const int vs = j % VST;
         mbar_wait(&bar.p_ready[sb], (j / NSB) & 1, wc);
@@ -229,30 +244,69 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tc_fence_after();
         const uint64_t dv = dv0 + vs * stage_step(TILE_BYTES);
         const uint32_t ta = tmem + TM_S0 + sb * BN;
+        if (empty == 0) {
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-          umma_bf16_ts(tmem + TM_O, ta + kk * 8, dv + mnmajor_step(kk), IDESC_PV,
-                       (j > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < BN / 16; ++kk)
+            umma_bf16_ts(tmem + TM_O, ta + kk * 8, dv + mnmajor_step(kk), IDESC_PV,
+                         (j > 0 || kk > 0) ? 1u : 0u);
+        } else {
+          // the four k-steps of the other key half only
+          const int k0 = empty == 1 ? 4 : 0;
+#pragma unroll
+          for (int kk = 0; kk < BN / 32; ++kk)
+            umma_bf16_ts(tmem + TM_O, ta + (k0 + kk) * 8, dv + mnmajor_step(k0 + kk), IDESC_PV,
+                         (j > 0 || kk > 0) ? 1u : 0u);
+        }
         umma_commit(&bar.pv_done[sb]);
         umma_commit(&bar.v_empty[vs]);
       };
-      mbar_wait(&bar.q_full, 0, wc);
-      for (int n = 0; n < n_tiles; ++n) {
+      auto issue_s = [&](int n, int empty) {
         const int sb = n % NSB;
         const int ks = n % KST;
         mbar_wait(&bar.k_full[ks], (n / KST) & 1, wc);
         tc_fence_after();
         const uint64_t dk = dk0 + ks * stage_step(TILE_BYTES);
         const uint32_t td = tmem + TM_S0 + sb * BN;
+        if (empty == 0) {
 #pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk)
-          umma_bf16_ss(td, dq0 + kmajor_step(kk, HALF_BYTES), dk + kmajor_step(kk, HALF_BYTES),
-                       IDESC_QK, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < HD / 16; ++kk)
+            umma_bf16_ss(td, dq0 + kmajor_step(kk, HALF_BYTES), dk + kmajor_step(kk, HALF_BYTES),
+                         IDESC_QK, kk > 0 ? 1u : 0u);
+        } else {
+          // one key half only: its 64 K rows into its 64 S columns
+          const int hf = empty == 1 ? 1 : 0;
+#pragma unroll
+          for (int kk = 0; kk < HD / 16; ++kk)
+            umma_bf16_ss(td + hf * 64, dq0 + kmajor_step(kk, HALF_BYTES),
+                         dk + hf * ROWS64_STEP + kmajor_step(kk, HALF_BYTES), IDESC_QK_HALF,
+                         kk > 0 ? 1u : 0u);
+        }
         umma_commit(&bar.s_full[sb]);
         umma_commit(&bar.k_empty[ks]);
-        if (n >= 2) issue_pv(n - 2);
+      };
+      mbar_wait(&bar.q_full, 0, wc);
+      if (!halves) {
+        for (int n = 0; n < n_tiles; ++n) {
+          issue_s(n, 0);
+          if (n >= 2) issue_pv(n - 2, 0);
+        }
+        for (int j = max(0, n_tiles - 2); j < n_tiles; ++j) issue_pv(j, 0);
+      } else {
+        // The flags reach the issuer one tile ahead of use (a load consumed right away
+        // holds the issue of the next MMAs back) and stay in a register history, two
+        // bits per tile, for the PV MMA two tiles later.
+        int e_next = n_tiles > 0 ? __ldg(pl.kt_cls + beg) : 0;
+        uint32_t hist = 0u;
+        for (int n = 0; n < n_tiles; ++n) {
+          const int empty = entry_empty_halves(e_next);
+          hist = (hist << 2) | static_cast<uint32_t>(empty);
+          if (n + 1 < n_tiles) e_next = __ldg(pl.kt_cls + beg + n + 1);
+          issue_s(n, empty);
+          if (n >= 2) issue_pv(n - 2, (hist >> 4) & 3);
+        }
+        for (int j = max(0, n_tiles - 2); j < n_tiles; ++j)
+          issue_pv(j, (hist >> (2 * (n_tiles - 1 - j))) & 3);
       }
-      for (int j = max(0, n_tiles - 2); j < n_tiles; ++j) issue_pv(j);
     }
   } else {
     // ------------------------------------------------ softmax warps 0-7
@@ -269,38 +323,47 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     float m_run = -INFINITY;
     float l_run = 0.f;
 
-    for (int n = 0; n < n_tiles; ++n) {
+    // One key tile; IDLE: this warp's key half holds no pair of the tile (no S to read,
+    // no P to write, only the row-max exchange and the O rescale).  Two instantiations
+    // keep the common path's code exactly that of a full-width tile.
+    auto tile_step = [&](int n, auto idle_c) {
+      constexpr bool IDLE = decltype(idle_c)::value;
       const int st = n % NSB;             // S buffer
       const uint32_t ph = (n / NSB) & 1;
       const int rp = n & 1;               // max-exchange parity
-      const int kt = __ldg(pl.kt_idx + beg + n);
-      const int cls = __ldg(pl.kt_cls + beg + n);
-      const int c0 = kt * BN + half * 64;
-      const bool masked = cls != LCA_TILE_FULL || kt * BN + BN > S;
-      uint32_t bits[2] = {0u, 0u};
-      if (masked && i < S) row_tile_bits<2>(a.mask, hm, i, c0, sp, bits, &mcur);
-      mbar_wait(&bar.s_full[st], ph, wc);
-      __syncwarp();
-      tc_fence_after();
-      uint32_t r[64];
-      tmem_ld64(lane_addr + TM_S0 + st * BN, r);
       float s[64];
+      float mx = -INFINITY;
+      if constexpr (!IDLE) {
+        const int kt = __ldg(pl.kt_idx + beg + n);
+        const int e = __ldg(pl.kt_cls + beg + n);
+        const int c0 = kt * BN + half * 64;
+        const bool masked = entry_class(e) != LCA_TILE_FULL || kt * BN + BN > S;
+        uint32_t bits[2] = {0u, 0u};
+        if (masked && i < S) row_tile_bits<2>(a.mask, hm, i, c0, sp, bits, &mcur);
+        mbar_wait(&bar.s_full[st], ph, wc);
+        __syncwarp();
+        tc_fence_after();
+        uint32_t r[64];
+        tmem_ld64(lane_addr + TM_S0 + st * BN, r);
 #pragma unroll
-      for (int x = 0; x < 64; ++x) s[x] = __uint_as_float(r[x]);
-      if (masked) {
+        for (int x = 0; x < 64; ++x) s[x] = __uint_as_float(r[x]);
+        if (masked) {
 #pragma unroll
-        for (int x = 0; x < 64; ++x)
-          if (!((bits[x >> 5] >> (x & 31)) & 1u)) s[x] = -INFINITY;
+          for (int x = 0; x < 64; ++x)
+            if (!((bits[x >> 5] >> (x & 31)) & 1u)) s[x] = -INFINITY;
+        }
+        float mq[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mq[k] = s[k];
+#pragma unroll
+        for (int x = 8; x < 64; x += 8)
+#pragma unroll
+          for (int k = 0; k < 8; ++k) mq[k] = fmaxf(mq[k], s[x + k]);
+        mx = fmaxf(fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])),
+                   fmaxf(fmaxf(mq[4], mq[5]), fmaxf(mq[6], mq[7])));
+      } else {
+        mbar_wait(&bar.s_full[st], ph, wc);
       }
-      float mq[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) mq[k] = s[k];
-#pragma unroll
-      for (int x = 8; x < 64; x += 8)
-#pragma unroll
-        for (int k = 0; k < 8; ++k) mq[k] = fmaxf(mq[k], s[x + k]);
-      float mx = fmaxf(fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])),
-                       fmaxf(fmaxf(mq[4], mq[5]), fmaxf(mq[6], mq[7])));
       red[(rp * 2 + half) * BM + t] = mx;
       named_bar_sync(BAR_SOFTMAX, SOFTMAX_THREADS);
       mx = fmaxf(mx, red[(rp * 2 + (half ^ 1)) * BM + t]);
@@ -326,24 +389,36 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         for (int x = 0; x < OCOLS; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * f);
         tmem_stn<OCOLS>(quarter_addr + TM_O + half * OCOLS, o);
       }
-      const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-      float ls[8];
+      if constexpr (!IDLE) {
+        const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+        float ls[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) ls[k] = 0.f;
+        for (int k = 0; k < 8; ++k) ls[k] = 0.f;
 #pragma unroll
-      for (int x = 0; x < 64; ++x) {
-        s[x] = ex2_approx(fmaf(s[x], sl2, -m_use));
-        ls[x & 7] += s[x];
+        for (int x = 0; x < 64; ++x) {
+          s[x] = ex2_approx(fmaf(s[x], sl2, -m_use));
+          ls[x & 7] += s[x];
+        }
+        l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+        // P (bf16 pairs) into the first 64 columns of this S buffer; both halves of the
+        // row finished reading S before the max exchange barrier above
+        uint32_t pk[32];
+#pragma unroll
+        for (int x = 0; x < 32; ++x) pk[x] = pack_bf16x2(s[2 * x], s[2 * x + 1]);
+        tmem_st32(quarter_addr + TM_S0 + st * BN + half * 32, pk);
       }
-      l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
-      // P (bf16 pairs) into the first 64 columns of this S buffer; both halves of the
-      // row finished reading S before the max exchange barrier above
-      uint32_t pk[32];
-#pragma unroll
-      for (int x = 0; x < 32; ++x) pk[x] = pack_bf16x2(s[2 * x], s[2 * x + 1]);
-      tmem_st32(quarter_addr + TM_S0 + st * BN + half * 32, pk);
       tc_fence_before();
       mbar_arrive(&bar.p_ready[st]);
+    };
+    if (!use_half_path(pl.kt_cls + beg, n_tiles, HALF_SHARE, lane)) {
+      for (int n = 0; n < n_tiles; ++n) tile_step(n, std::false_type{});
+    } else {
+      for (int n = 0; n < n_tiles; ++n) {
+        if ((entry_empty_halves(__ldg(pl.kt_cls + beg + n)) >> half) & 1)
+          tile_step(n, std::true_type{});
+        else
+          tile_step(n, std::false_type{});
+      }
     }
 
     // ---- epilogue: O = acc / l (bf16), LSE = (m + log2 l) * ln 2

@@ -382,6 +382,37 @@ __device__ __forceinline__ int seg_find_from(const int32_t* cu, int n, int hint,
   return lo;
 }
 
+// Tile bytes of the plan (class in bits 0-1, empty-half flags in bits 2-5) and the
+// entries of its row and column lists.
+__host__ __device__ __forceinline__ uint8_t row_list_byte(uint8_t c) {
+  return static_cast<uint8_t>(c & 15);
+}
+__host__ __device__ __forceinline__ uint8_t col_list_byte(uint8_t c) {
+  return static_cast<uint8_t>((c & LCA_TILE_CLASS_MASK) | ((c >> 4) << 2));
+}
+// Empty halves of a list entry: bit 0 the first half, bit 1 the second (key columns
+// in a row list, query rows in a column list).
+__device__ __forceinline__ int entry_empty_halves(int e) { return (e >> 2) & 3; }
+__device__ __forceinline__ int entry_class(int e) { return e & LCA_TILE_CLASS_MASK; }
+
+// Whether a list of n plan entries runs the half-width path: it is long (at least 64
+// entries) and at least 1/share of its entries flag an empty half.  The flag-aware loops
+// cost a few percent per tile over the plain ones, and short lists are bound by load
+// and MMA round-trip latency, where half-width tiles were measured slower; other lists
+// run the plain loops (which treat a flagged tile as a partial full-width one).  The
+// forward passes share 4, the backward kernels (whose half-width tiles save less) 2.
+// The MMA issuer and the softmax warps of a CTA decide alike.
+__device__ __forceinline__ bool half_path(int flagged, int n, int share) {
+  return n >= 64 && share * flagged >= n;
+}
+// half_path over the n entries at e.  Warp-wide: every lane calls it and gets the same
+// answer.
+__device__ __forceinline__ bool use_half_path(const uint8_t* e, int n, int share, int lane) {
+  int f = 0;
+  for (int x = lane; x < n; x += 32) f += (__ldg(e + x) & 12) != 0;
+  return half_path(__reduce_add_sync(0xFFFFFFFFu, f), n, share);
+}
+
 // Per-thread search hints of the variable block-sparse map: the row block of the last
 // row and the column block of the last column window looked up.  Only speed depends
 // on them; start them at -1.

@@ -4,8 +4,10 @@
 // context-parallel framework precomputes its metadata once per mask
 // ("Long-Context Attention Benchmark", summary page section 2.2; reading note, "Key
 // design" 2-3).  Here that representation is a tile plan:
-//   classify  - every (query tile, key tile) pair -> SKIP / FULL / PARTIAL, plus the
-//               exact number of allowed pairs per map head and the list lengths;
+//   classify  - every (query tile, key tile) pair -> SKIP / FULL / PARTIAL and, for a
+//               non-skipped tile, which of its key-column and query-row halves hold
+//               no allowed pair (a kernel leaves those halves out), plus the exact
+//               number of allowed pairs per map head and the list lengths;
 //   scan      - CSR row pointers per (map head, query tile) and column pointers per
 //               (map head, key tile);
 //   fill      - ascending key-tile lists per row and query-tile lists per column;
@@ -36,7 +38,7 @@ __global__ void __launch_bounds__(TQ) classify_kernel(MaskDev m, int n_qt, int n
                                                       unsigned long long* n_partial) {
   constexpr int NWARP = TQ / 32;
   constexpr int NW = TK / 32;
-  __shared__ uint8_t s_any[NWARP][KT_CHUNK];
+  __shared__ uint8_t s_any[NWARP][KT_CHUNK];   // bit 0 / 1: a pair in key half 0 / 1
   __shared__ uint8_t s_all[NWARP][KT_CHUNK];
   __shared__ unsigned long long s_red[NWARP];
   __shared__ int s_len[NWARP];
@@ -87,37 +89,52 @@ __global__ void __launch_bounds__(TQ) classify_kernel(MaskDev m, int n_qt, int n
       }
       const int c0 = kt * TK;
       const int width = min(TK, S - c0);
-      int cnt = 0;
+      const int cm = c0 + TK / 2;          // first key column of the second half
+      int cnt0 = 0, cnt1 = 0;              // allowed pairs of this row in each key half
       if (valid) {
         if (sparse) {
           uint32_t bits[NW];
           row_tile_bits<NW>(m, hm, i, c0, sp, bits, &mcur);
 #pragma unroll
-          for (int w = 0; w < NW; ++w) cnt += __popc(bits[w]);
+          for (int w = 0; w < NW; ++w) (w < NW / 2 ? cnt0 : cnt1) += __popc(bits[w]);
         } else {
-          cnt = overlap(sp.a0, sp.b0, c0, c0 + width) + overlap(sp.a1, sp.b1, c0, c0 + width);
+          const int ce = c0 + width;
+          cnt0 = overlap(sp.a0, sp.b0, c0, min(cm, ce)) + overlap(sp.a1, sp.b1, c0, min(cm, ce));
+          cnt1 = overlap(sp.a0, sp.b0, cm, ce) + overlap(sp.a1, sp.b1, cm, ce);
         }
       }
+      const int cnt = cnt0 + cnt1;
       my_count += static_cast<unsigned long long>(cnt);
-      const bool any_w = __any_sync(0xFFFFFFFFu, valid && cnt > 0);
+      const bool any0 = __any_sync(0xFFFFFFFFu, valid && cnt0 > 0);
+      const bool any1 = __any_sync(0xFFFFFFFFu, valid && cnt1 > 0);
       const bool all_w = __all_sync(0xFFFFFFFFu, !valid || cnt == width);
       if (lane == 0) {
-        s_any[warp][kt - k0] = any_w;
+        s_any[warp][kt - k0] = static_cast<uint8_t>(any0 | (any1 << 1));
         s_all[warp][kt - k0] = all_w;
       }
     }
     __syncthreads();
     for (int kt = k0 + threadIdx.x; kt < k1; kt += TQ) {
-      bool a = false, f = true;
+      int keys = 0, top = 0, bottom = 0;   // key halves with a pair; rows of each half
+      bool f = true;
 #pragma unroll
       for (int w = 0; w < NWARP; ++w) {
-        a = a || s_any[w][kt - k0];
+        const int x = s_any[w][kt - k0];
+        keys |= x;
+        (w < NWARP / 2 ? top : bottom) |= x;
         f = f && s_all[w][kt - k0];
       }
-      const uint8_t c = !a ? LCA_TILE_SKIP : (f ? LCA_TILE_FULL : LCA_TILE_PARTIAL);
+      uint8_t c = LCA_TILE_SKIP;
+      if (keys != 0) {
+        c = f ? LCA_TILE_FULL : LCA_TILE_PARTIAL;
+        if (!(keys & 1)) c |= LCA_TILE_KEY_HALF0_EMPTY;
+        if (!(keys & 2)) c |= LCA_TILE_KEY_HALF1_EMPTY;
+        if (!top) c |= LCA_TILE_QUERY_HALF0_EMPTY;
+        if (!bottom) c |= LCA_TILE_QUERY_HALF1_EMPTY;
+      }
       cls_row[kt] = c;
       my_len += (c != LCA_TILE_SKIP);
-      my_part += (c == LCA_TILE_PARTIAL);
+      my_part += ((c & LCA_TILE_CLASS_MASK) == LCA_TILE_PARTIAL);
     }
     __syncthreads();
   }
@@ -209,7 +226,7 @@ __global__ void fill_rows_kernel(const uint8_t* cls, int n_rows, int n_kt, const
     if (c != 0) {
       const int at = pos + __popc(bal & ((1u << lane) - 1u));
       kt_idx[at] = kt;
-      kt_cls[at] = c;
+      kt_cls[at] = row_list_byte(c);
     }
     pos += __popc(bal);
   }
@@ -227,7 +244,7 @@ __global__ void fill_cols_kernel(const uint8_t* cls, int map_heads, int n_qt, in
     const uint8_t v = base[static_cast<size_t>(qt) * n_kt];
     if (v) {
       qt_idx[pos] = qt;
-      qt_cls[pos] = v;
+      qt_cls[pos] = col_list_byte(v);
       ++pos;
     }
   }

@@ -23,7 +23,7 @@ def _compare(desc, tq, tk):
         assert got["n_valid"][hm] == oracle.n_valid_popcount(desc, hm), f"{desc.name} n_valid"
     info = plan.info
     assert info["nnz"] == len(ref["kt_idx"])
-    assert info["n_partial"] == int((ref["cls"] == 2).sum())
+    assert info["n_partial"] == int(((ref["cls"] & 3) == 2).sum())
 
 
 @pytest.mark.parametrize("s", [1000, 1408])
@@ -31,6 +31,21 @@ def _compare(desc, tq, tk):
 def test_plan_bit_exact_all_masks(s, tiles):
     for desc in small_descs(s, hq=4, hkv=2, seed=s):
         _compare(desc, *tiles)
+
+
+@pytest.mark.parametrize("s", [1344, 950])
+def test_plan_half_flags(s):
+    # 64-token blocks against 128 tiles, and ragged tails whose second half is past S
+    for seed, sp in ((1, 0.5), (2, 0.8)):
+        _compare(I.make_desc(I.BLOCK_SPARSE_UNIFORM, s, sparse_block=64, sparsity=sp,
+                             map_heads=2, map_seed=seed), 128, 128)
+    _compare(I.make_desc(I.CAUSAL, s), 128, 128)
+    _compare(I.make_desc(I.FULL, s), 128, 64)
+    got = lca.mask_build(I.make_desc(I.BLOCK_SPARSE_UNIFORM, s, sparse_block=64, sparsity=0.5,
+                                     map_heads=2, map_seed=1), 128, 128).export()
+    flags = got["cls"][got["cls"] != 0] >> 2
+    for bit in (1, 2, 4, 8):   # every flag occurs
+        assert (flags & bit).any(), bit
 
 
 def test_plan_degenerate_cases():
@@ -57,9 +72,11 @@ def _check_internal(got, n_qt, n_kt, hm_n):
     cols = np.transpose(cls, (0, 2, 1)).reshape(hm_n * n_kt, n_qt)
     assert np.array_equal(np.diff(got["colptr"]), np.count_nonzero(cols, axis=1))
     nz_r = np.nonzero(rows)
-    assert np.array_equal(got["kt_idx"], nz_r[1]) and np.array_equal(got["kt_cls"], rows[nz_r])
+    assert np.array_equal(got["kt_idx"], nz_r[1])
+    assert np.array_equal(got["kt_cls"], oracle.row_list_byte(rows[nz_r]))
     nz_c = np.nonzero(cols)
-    assert np.array_equal(got["qt_idx"], nz_c[1]) and np.array_equal(got["qt_cls"], cols[nz_c])
+    assert np.array_equal(got["qt_idx"], nz_c[1])
+    assert np.array_equal(got["qt_cls"], oracle.col_list_byte(cols[nz_c]))
     for key, ptr in (("work_q", "rowptr"), ("work_k", "colptr")):
         ln = np.diff(got[ptr])
         w = got[key]
