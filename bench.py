@@ -521,12 +521,14 @@ def run_gpu(args, rank, world):
         w_ms = ev[2].elapsed_time(ev[3])
         acc = per_cfg.setdefault(case_label(args.suite, s, hq, hkv, name),
                                  {"fwd": [], "bwd": [], "build_ms": [], "fwd_ms": [],
-                                  "bwd_ms": [], "info": info, "hq": hq, "gi": gi, "s": s})
+                                  "bwd_ms": [], "pairs": [], "info": info, "hq": hq, "gi": gi,
+                                  "s": s})
         acc["fwd"].append(tflops(FWD_PER_PAIR * hp, f_ms))
         acc["bwd"].append(tflops(BWD_PER_PAIR * hp, w_ms))
         acc["build_ms"].append(b_ms)
         acc["fwd_ms"].append(f_ms)
         acc["bwd_ms"].append(w_ms)
+        acc["pairs"].append(hp)
     per_config = {}
     for label, v in per_cfg.items():
         fwd, bwd = statistics.median(v["fwd"]), statistics.median(v["bwd"])
@@ -542,6 +544,9 @@ def run_gpu(args, rank, world):
             row.update({"fwd_ms": round(f_ms, 3), "bwd_ms": round(w_ms, 3),
                         "nonskipped_tile_fraction":
                             round(inf["nnz"] / (inf["map_heads"] * inf["n_qt"] * inf["n_kt"]), 4),
+                        # allowed pairs per pair of the non-skipped tiles (partial-tile waste)
+                        "tile_efficiency": round(statistics.median(v["pairs"]) /
+                                                 (head_tiles * 128 * 128), 4),
                         "fwd_us_per_head_tile": round(1e3 * f_ms / head_tiles, 4),
                         "bwd_us_per_head_tile": round(1e3 * w_ms / head_tiles, 4)})
         per_config[label] = row

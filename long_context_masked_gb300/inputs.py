@@ -58,10 +58,18 @@ MASK_NAMES = {
     SLIDING_WINDOW_DOCUMENT: "SLIDING_WINDOW_DOCUMENT",
 }
 
-# Tile classes written by the mask builder (lca_tile_class).
+# Tile classes written by the mask builder (lca_tile_class), and the empty-half flags of a
+# non-skipped tile's byte (a half without any allowed in-range pair).  Row-list entries
+# (kt_cls) carry the class and the key-half flags; column-list entries (qt_cls) carry the
+# class and the query-half flags moved down to 4 / 8.
 TILE_SKIP = 0
 TILE_FULL = 1
 TILE_PARTIAL = 2
+TILE_CLASS_MASK = 3
+TILE_KEY_HALF0_EMPTY = 4
+TILE_KEY_HALF1_EMPTY = 8
+TILE_QUERY_HALF0_EMPTY = 16
+TILE_QUERY_HALF1_EMPTY = 32
 
 
 @dataclasses.dataclass

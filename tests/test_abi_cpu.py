@@ -7,6 +7,7 @@ import re
 import pytest
 
 from long_context_masked_gb300 import binding
+from long_context_masked_gb300 import inputs as I
 from long_context_masked_gb300 import build as lca_build
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -107,3 +108,17 @@ def test_block_map_entry_points_validate_before_launch(lib):
     assert lib.lca_block_topk(p, 2, 3, 10, 11, p, None) == 1
     assert lib.lca_block_topk(None, 2, 3, 10, 4, p, None) == 1
     assert lib.lca_block_topk(p, 0, 3, 10, 4, p, None) == 1
+
+
+def test_python_constants_match_the_header():
+    """The binding's enum values are the header's (tile classes and empty-half flags,
+    mask types)."""
+    with open(os.path.join(ROOT, "include", "lca.h")) as f:
+        hdr = f.read()
+    vals = {m.group(1): int(m.group(2)) for m in re.finditer(r"\bLCA_([A-Z0-9_]+)\s*=\s*(\d+)", hdr)}
+    for name in ("TILE_SKIP", "TILE_FULL", "TILE_PARTIAL", "TILE_CLASS_MASK",
+                 "TILE_KEY_HALF0_EMPTY", "TILE_KEY_HALF1_EMPTY", "TILE_QUERY_HALF0_EMPTY",
+                 "TILE_QUERY_HALF1_EMPTY"):
+        assert getattr(I, name) == vals[name], name
+    for t, name in I.MASK_NAMES.items():
+        assert vals[name] == t, name
