@@ -44,10 +44,20 @@ def test_plan_consistent_with_mask(seed):
     cu = I.cu_from_lengths(I.lognormal_doc_lengths(s, seed, mu=np.log(40), lo=5))
     bm = I.uniform_block_map(s, 8, 3, 0.6, seed)
     ro, co, vm = I.variable_block_map(s, 2, seed)
+    q = max(1, s // 7)
+    rest = s - q
     descs = [
         I.MaskDesc(I.CAUSAL, s), I.MaskDesc(I.FULL, s),
         I.MaskDesc(I.SLIDING_WINDOW, s, window=37),
+        I.MaskDesc(I.FULL_DOCUMENT, s, cu_seqlens=cu),
         I.MaskDesc(I.CAUSAL_DOCUMENT, s, cu_seqlens=cu),
+        I.MaskDesc(I.SLIDING_WINDOW_DOCUMENT, s, window=23, cu_seqlens=cu),
+        I.MaskDesc(I.PREFIX_LM, s, prefix_len=s // 4),
+        I.MaskDesc(I.SHARED_QUESTION, s,
+                   cu_seqlens=np.array([0, q, q + rest // 2, s], np.int32)),
+        I.MaskDesc(I.GLOBAL_SLIDING, s, num_global=5, window=29),
+        I.MaskDesc(I.GLOBAL_SLIDING, s, num_global=5, window=29, base_causal=0),
+        I.MaskDesc(I.CAUSAL_BLOCKWISE, s, block=19),
         I.MaskDesc(I.BLOCK_CAUSAL_DOCUMENT, s, block=12, cu_seqlens=cu),
         I.MaskDesc(I.BLOCK_SPARSE_UNIFORM, s, block=8, map_heads=3, block_map=bm,
                    n_row_blocks=bm.shape[1], n_col_blocks=bm.shape[2]),
