@@ -141,7 +141,8 @@ class Plan:
         return self._h
 
     def export(self) -> dict:
-        """Host copies of every plan array."""
+        """Host copies of every plan array.  ``cls`` holds the tile bytes (class in bits 0-1,
+        empty-half flags above: inputs.TILE_*), ``kt_cls`` / ``qt_cls`` the list entries."""
         inf = self.info
         hm, nq, nk, nnz = inf["map_heads"], inf["n_qt"], inf["n_kt"], inf["nnz"]
         out = {"cls": np.zeros(hm * nq * nk, np.uint8), "rowptr": np.zeros(hm * nq + 1, np.int32),
