@@ -259,7 +259,8 @@ __device__ __forceinline__ bool walk_use_half_path(const PlanDev& pl, int kt, in
     prev = col;
     const int p0 = __ldg(pl.colptr + col), p1 = __ldg(pl.colptr + col + 1);
     n += p1 - p0;
-    for (int x = p0 + lane; x < p1; x += 32) f += (__ldg(pl.qt_cls + x) & 12) != 0;
+    for (int x = p0 + lane; x < p1; x += 32)
+      f += (__ldg(pl.qt_cls + x) & kEntryHalfFlags) != 0;
   }
   return half_path(__reduce_add_sync(0xFFFFFFFFu, f), n, HALF_SHARE);
 }

@@ -385,7 +385,8 @@ __device__ __forceinline__ int seg_find_from(const int32_t* cu, int n, int hint,
 // Tile bytes of the plan (class in bits 0-1, empty-half flags in bits 2-5) and the
 // entries of its row and column lists.
 __host__ __device__ __forceinline__ uint8_t row_list_byte(uint8_t c) {
-  return static_cast<uint8_t>(c & 15);
+  return static_cast<uint8_t>(c & (LCA_TILE_CLASS_MASK | LCA_TILE_KEY_HALF0_EMPTY |
+                                   LCA_TILE_KEY_HALF1_EMPTY));
 }
 __host__ __device__ __forceinline__ uint8_t col_list_byte(uint8_t c) {
   return static_cast<uint8_t>((c & LCA_TILE_CLASS_MASK) | ((c >> 4) << 2));
@@ -394,6 +395,8 @@ __host__ __device__ __forceinline__ uint8_t col_list_byte(uint8_t c) {
 // in a row list, query rows in a column list).
 __device__ __forceinline__ int entry_empty_halves(int e) { return (e >> 2) & 3; }
 __device__ __forceinline__ int entry_class(int e) { return e & LCA_TILE_CLASS_MASK; }
+// Both empty-half flags of a list entry (bits 2-3 in row and column lists alike).
+constexpr int kEntryHalfFlags = LCA_TILE_KEY_HALF0_EMPTY | LCA_TILE_KEY_HALF1_EMPTY;
 
 // Whether a list of n plan entries runs the half-width path: it is long (at least 64
 // entries) and at least 1/share of its entries flag an empty half.  The flag-aware loops
@@ -409,7 +412,7 @@ __device__ __forceinline__ bool half_path(int flagged, int n, int share) {
 // answer.
 __device__ __forceinline__ bool use_half_path(const uint8_t* e, int n, int share, int lane) {
   int f = 0;
-  for (int x = lane; x < n; x += 32) f += (__ldg(e + x) & 12) != 0;
+  for (int x = lane; x < n; x += 32) f += (__ldg(e + x) & kEntryHalfFlags) != 0;
   return half_path(__reduce_add_sync(0xFFFFFFFFu, f), n, share);
 }
 
