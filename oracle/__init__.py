@@ -34,7 +34,7 @@ masks.  No function is left unpinned.
 from . import masks, attention, plan, counts, blockmap  # noqa: F401
 from .masks import allowed, mask_rows, materialize_mask, map_head_of  # noqa: F401
 from .attention import (attn_fwd_ref, attn_bwd_ref, attn_fwd_rows_ref,  # noqa: F401
-                        attn_dq_rows_ref)
+                        attn_dq_rows_ref, attn_dkdv_cols_ref)
 from .plan import col_list_byte, row_list_byte, tile_plan_ref, tile_rows_ref  # noqa: F401
 from .counts import n_valid_popcount, n_valid_closed_form  # noqa: F401
 from .blockmap import topk_count, topk_block_map, pooled_block_scores  # noqa: F401

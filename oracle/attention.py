@@ -36,7 +36,7 @@ from typing import Optional, Sequence
 
 import numpy as np
 
-from .masks import mask_rows, map_head_of
+from .masks import allowed, mask_rows, map_head_of
 
 
 def _default_scale(d: int, scale: Optional[float]) -> float:
@@ -174,3 +174,48 @@ def attn_dq_rows_ref(q, k, v, do, desc, *, heads: Sequence[int], rows: Sequence[
         dd[a] = (p * dp).sum(axis=1)
         dq[a] = sc * ((p * (dp - dd[a][:, None])) @ kk)
     return dq, o, lse, dd
+
+
+def attn_dkdv_cols_ref(q, k, v, do, desc, *, kv_heads: Sequence[int], cols: Sequence[int],
+                       batch: int = 0, scale: Optional[float] = None, chunk: int = 2048):
+    """dK and dV at selected key positions of selected KV heads, fp64.
+
+    For key j of KV head hk, summed over the query heads h of its group:
+    dV_j = sum_i P_ij dO_i and dK_j = scale * sum_i dS_ij q_i with
+    dS_ij = P_ij (dP_ij - D_i).  P_ij and dS_ij vanish unless M_ij, so only the
+    query rows that may attend at least one selected key are evaluated; each of
+    those rows is evaluated over all keys (which gives its LSE_i and D_i).  This
+    is the attn_bwd_ref arithmetic restricted to the rows and columns that reach
+    the selected keys, for checks at sizes where the full backward is too slow.
+
+    Returns ``(dK [len(kv_heads), len(cols), d], dV [len(kv_heads), len(cols), d])``.
+    """
+    _, s_len, h_q, d = q.shape
+    h_kv = k.shape[2]
+    g = h_q // h_kv
+    sc = _default_scale(d, scale)
+    cols = np.asarray(cols, np.int64)
+    all_rows = np.arange(s_len, dtype=np.int64)
+    dk = np.zeros((len(kv_heads), len(cols), d))
+    dv = np.zeros((len(kv_heads), len(cols), d))
+    for a, hk in enumerate(kv_heads):
+        kk = np.asarray(k[batch, :, hk, :], np.float64)
+        vv = np.asarray(v[batch, :, hk, :], np.float64)
+        for h in range(hk * g, (hk + 1) * g):
+            hm = map_head_of(h, h_q, h_kv, desc.map_heads)
+            reach = np.broadcast_to(allowed(desc, hm, all_rows[:, None], cols[None, :]),
+                                    (s_len, len(cols)))
+            rows = np.nonzero(reach.any(axis=1))[0]
+            for r0 in range(0, len(rows), chunk):
+                rr = rows[r0:r0 + chunk]
+                qq = np.asarray(q[batch, rr, h, :], np.float64)
+                gg = np.asarray(do[batch, rr, h, :], np.float64)
+                m = mask_rows(desc, hm, rr)
+                _, p = _row_softmax(sc * (qq @ kk.T), m)
+                dp = gg @ vv.T
+                d_rows = (p * dp).sum(axis=1)
+                p_c = p[:, cols]
+                ds_c = p_c * (dp[:, cols] - d_rows[:, None])
+                dv[a] += p_c.T @ gg
+                dk[a] += sc * (ds_c.T @ qq)
+    return dk, dv

@@ -258,3 +258,63 @@ def test_row_range_restriction_is_a_slice_of_the_full_result():
                                atol=1e-13)
     np.testing.assert_allclose(parts[0]["dK"] + parts[1]["dK"], full["dK"], atol=1e-13)
     np.testing.assert_allclose(parts[0]["dV"] + parts[1]["dV"], full["dV"], atol=1e-13)
+
+
+def test_key_column_function_matches_finite_differences():
+    """dK/dV at selected keys equal the numerical gradient of L = sum(O * dO) with
+    respect to those key and value rows (independent of attn_bwd_ref)."""
+    rng = np.random.default_rng(23)
+    s, d, hq, hkv = 12, 3, 4, 2
+    desc = I.MaskDesc(I.CAUSAL_DOCUMENT, s, cu_seqlens=np.array([0, 5, 12], np.int32))
+    q, do = _rand((1, s, hq, d), rng), _rand((1, s, hq, d), rng)
+    k, v = _rand((1, s, hkv, d), rng), _rand((1, s, hkv, d), rng)
+    sc = 0.7
+    cols, kv_heads = [0, 4, 5, 11], [1, 0]
+    dk, dv = oracle.attn_dkdv_cols_ref(q, k, v, do, desc, kv_heads=kv_heads, cols=cols, scale=sc)
+
+    def loss(k_, v_):
+        o, _ = oracle.attn_fwd_ref(q, k_, v_, desc, scale=sc)
+        return float((o * do).sum())
+
+    eps = 1e-6
+    for a, hk in enumerate(kv_heads):
+        for c, j in enumerate(cols):
+            for x in range(d):
+                for name, got in (("k", dk), ("v", dv)):
+                    kp, km, vp, vm = k.copy(), k.copy(), v.copy(), v.copy()
+                    if name == "k":
+                        kp[0, j, hk, x] += eps
+                        km[0, j, hk, x] -= eps
+                    else:
+                        vp[0, j, hk, x] += eps
+                        vm[0, j, hk, x] -= eps
+                    num = (loss(kp, vp) - loss(km, vm)) / (2 * eps)
+                    assert abs(got[a, c, x] - num) <= 1e-7 + 1e-6 * abs(num), (name, hk, j, x)
+
+
+@pytest.mark.parametrize("mask", [I.FULL, I.SLIDING_WINDOW, I.SHARED_QUESTION,
+                                  I.BLOCK_SPARSE_UNIFORM, I.BLOCK_SPARSE_VARIABLE])
+def test_key_column_function_matches_full_backward(mask):
+    """Restricting the backward to the rows that reach the selected keys changes
+    nothing: every mask type, GQA with per-query-head maps, unreachable keys give 0."""
+    rng = np.random.default_rng(29 + mask)
+    s, d, hq, hkv = 90, 5, 4, 2
+    if mask == I.BLOCK_SPARSE_UNIFORM:
+        bm = I.uniform_block_map(s, 16, hq, 0.5, 3)
+        bm[:, :, 2] = 0                      # key block 2 is never attended
+        desc = I.MaskDesc(mask, s, block=16, map_heads=hq, n_row_blocks=bm.shape[1],
+                          n_col_blocks=bm.shape[2], block_map=bm)
+    elif mask == I.SHARED_QUESTION:
+        desc = I.make_desc(mask, s, question=20, answers=[30, 40])
+    else:
+        desc = I.make_desc(mask, s, window=17, map_heads=hkv, map_seed=5, doc_seed=5)
+    q, do = _rand((1, s, hq, d), rng), _rand((1, s, hq, d), rng)
+    k, v = _rand((1, s, hkv, d), rng), _rand((1, s, hkv, d), rng)
+    full = oracle.attn_bwd_ref(q, k, v, do, desc, chunk=31)
+    cols = [0, 1, 33, 34, 35, 60, 89]
+    dk, dv = oracle.attn_dkdv_cols_ref(q, k, v, do, desc, kv_heads=[0, 1], cols=cols, chunk=13)
+    for a in range(2):
+        np.testing.assert_allclose(dk[a], full["dK"][0, cols, a], atol=1e-12)
+        np.testing.assert_allclose(dv[a], full["dV"][0, cols, a], atol=1e-12)
+    if mask == I.BLOCK_SPARSE_UNIFORM:
+        assert (dk[:, 2:5] == 0).all() and (dv[:, 2:5] == 0).all()
