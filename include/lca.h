@@ -141,12 +141,17 @@ typedef struct {
 /* Tensor shape.  Q, O, dO, dQ: [batch, seqlen, h_q, head_dim] bf16 with row stride
  * *_row_stride elements between consecutive positions (>= h_q * head_dim, multiple of
  * 8), heads packed (stride head_dim), batch stride seqlen * row_stride.  K, V, dK, dV:
- * [batch, seqlen, h_kv, head_dim] likewise.  LSE and D: [batch, h_q, seqlen] fp32,
- * contiguous.  All base pointers 16-byte aligned.  Masks with segments or block maps
- * require batch == 1. */
+ * [batch, seqlen, h_kv, head_dim] likewise.  Every tensor has its own row stride, so
+ * inputs may be slices of a packed QKV (or KV) tensor while the gradients are separate
+ * buffers, or the other way round.  The four gradient-side strides are read by
+ * lca_attn_bwd only; 0 there means "the row stride of the matching input": dO as O,
+ * dQ as Q, dK as K, dV as V.  LSE and D: [batch, h_q, seqlen] fp32, contiguous.  All
+ * base pointers 16-byte aligned.  Masks with segments or block maps require
+ * batch == 1. */
 typedef struct {
   int32_t batch, seqlen, h_q, h_kv, head_dim;
   int64_t q_row_stride, k_row_stride, v_row_stride, o_row_stride;
+  int64_t do_row_stride, dq_row_stride, dk_row_stride, dv_row_stride;
 } lca_shape;
 
 typedef struct lca_plan lca_plan; /* opaque; owns its device buffers */
@@ -187,7 +192,10 @@ void lca_plan_destroy(lca_plan* plan);
 
 /* Forward: O (bf16) and LSE (fp32, natural log) for all heads and rows.
  * Requires head_dim 128 or 64, plan tile_q == 128, tile_k == 128, plan seqlen ==
- * shape->seqlen, plan map_heads in {1, h_kv, h_q}.  softmax_scale <= 0 means
+ * shape->seqlen, plan map_heads in {1, h_kv, h_q}; a plan with 64-row or 64-column tiles
+ * returns LCA_ERR_UNSUPPORTED (the attention kernels run 128 x 128 tiles only, and
+ * leave out the empty 64-row / 64-column halves of a tile instead: see the tile-byte
+ * flags above).  Reads q/k/v/o_row_stride only.  softmax_scale <= 0 means
  * 1/sqrt(head_dim). */
 lca_status lca_attn_fwd(const lca_plan* plan, const lca_shape* shape, const void* q,
                         const void* k, const void* v, void* o, float* lse, float softmax_scale,
@@ -235,9 +243,13 @@ lca_status lca_block_topk(const float* scores, int map_heads, int n_rows, int n_
 size_t lca_attn_bwd_workspace(const lca_plan* plan, const lca_shape* shape, int flags);
 
 /* Backward: dQ, dK, dV (bf16) from Q, K, V, O, dO and the forward's LSE.
- * Same preconditions as lca_attn_fwd; `workspace` is a caller-owned device buffer of
- * at least lca_attn_bwd_workspace() bytes (16-byte aligned).  The result is
- * deterministic (no floating-point atomics).  flags: reserved, pass 0. */
+ * Same preconditions as lca_attn_fwd, plus the gradient-side row strides of `shape`
+ * (dO read with do_row_stride; dQ, dK, dV written with dq/dk/dv_row_stride; each 0 or
+ * >= its heads * head_dim and a multiple of 8, else LCA_ERR_INVALID_ARG).  Every row of
+ * dQ, dK and dV below seqlen is written (zero where no pair reaches it); nothing else in
+ * their buffers is touched.  `workspace` is a caller-owned device buffer of at least
+ * lca_attn_bwd_workspace() bytes (16-byte aligned).  The result is deterministic (no
+ * floating-point atomics).  flags: reserved, pass 0. */
 lca_status lca_attn_bwd(const lca_plan* plan, const lca_shape* shape, const void* q,
                         const void* k, const void* v, const void* o, const void* dout,
                         const float* lse, void* dq, void* dk, void* dv, void* workspace,
@@ -257,8 +269,9 @@ lca_status lca_attn_bwd(const lca_plan* plan, const lca_shape* shape, const void
  * LCA_ERR_UNSUPPORTED without launching anything.  No cudaMalloc / cudaFree is made
  * (with lca_profile_enable on, the timing events of the launches come from a pool
  * that grows on first use).
- * The first call on a device looks the buffer's device address up (once per device,
- * with that device current); make that first call before any stream capture.
+ * The first call on a device looks the buffer's device address up (with that device
+ * current; again after the device's context was torn down and re-created, e.g. by
+ * cudaDeviceReset); make that first call before any stream capture.
  * Every call on a device shares the one buffer: each call overwrites every entry it
  * reads, so nothing needs clearing, but calls whose work overlaps on the GPU (other
  * streams, other threads) race on it and must be serialised by the caller. */

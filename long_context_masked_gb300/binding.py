@@ -41,7 +41,9 @@ class ShapeC(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int32), ("seqlen", ctypes.c_int32), ("h_q", ctypes.c_int32),
                 ("h_kv", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("q_row_stride", ctypes.c_int64), ("k_row_stride", ctypes.c_int64),
-                ("v_row_stride", ctypes.c_int64), ("o_row_stride", ctypes.c_int64)]
+                ("v_row_stride", ctypes.c_int64), ("o_row_stride", ctypes.c_int64),
+                ("do_row_stride", ctypes.c_int64), ("dq_row_stride", ctypes.c_int64),
+                ("dk_row_stride", ctypes.c_int64), ("dv_row_stride", ctypes.c_int64)]
 
 
 class PlanInfoC(ctypes.Structure):
@@ -213,15 +215,28 @@ def mask_build(desc: I.MaskDesc, tile_q: int = 128, tile_k: int = 128, stream=No
     return Plan(out.value, desc)
 
 
-def _shape(q, k, v, o):
+def _shape(q, k, v, o, do=None, dq=None, dk=None, dv=None):
+    """lca_shape of the given tensors.  Each tensor is [B, S, heads, d] with packed heads
+    and its own row stride (slices of a packed QKV tensor are fine); the gradient-side
+    strides are filled from dO/dQ/dK/dV when they are given."""
     b, s, hq, d = q.shape
     hkv = k.shape[2]
-    for name, t, h in (("q", q, hq), ("k", k, hkv), ("v", v, hkv), ("o", o, hq)):
+    named = (("q", q, hq), ("k", k, hkv), ("v", v, hkv), ("o", o, hq), ("do", do, hq),
+             ("dq", dq, hq), ("dk", dk, hkv), ("dv", dv, hkv))
+    for name, t, h in named:
+        if t is None:
+            continue
         if t.stride(3) != 1 or t.stride(2) != d or t.stride(0) != s * t.stride(1):
             raise LcaError(f"{name}: unsupported layout {tuple(t.stride())}", 1)
-        if t.shape[:2] != (b, s) or t.shape[2] != h or t.shape[3] != d:
+        if tuple(t.shape[:2]) != (b, s) or t.shape[2] != h or t.shape[3] != d:
             raise LcaError(f"{name}: shape {tuple(t.shape)}", 1)
-    return ShapeC(b, s, hq, hkv, d, q.stride(1), k.stride(1), v.stride(1), o.stride(1))
+        if t.device != q.device:
+            raise LcaError(f"{name}: on {t.device}, q on {q.device}", 1)
+    sh = ShapeC(b, s, hq, hkv, d, q.stride(1), k.stride(1), v.stride(1), o.stride(1))
+    for name, t, _ in named[4:]:
+        if t is not None:
+            setattr(sh, f"{name}_row_stride", t.stride(1))
+    return sh
 
 
 def attn_fwd(plan: Plan, q, k, v, scale: Optional[float] = None, out=None, lse=None,
@@ -247,12 +262,10 @@ def attn_bwd(plan: Plan, q, k, v, o, do, lse, scale: Optional[float] = None, dq=
     import torch
 
     lib = load_library()
-    if do.stride() != o.stride():
-        raise LcaError("dO must have the layout of O", 1)
-    sh = _shape(q, k, v, o)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
+    sh = _shape(q, k, v, o, do, dq, dk, dv)
     ws_bytes = lib.lca_attn_bwd_workspace(plan.handle, ctypes.byref(sh), 0)
     if workspace is None:
         workspace = torch.empty(max(1, ws_bytes // 4), dtype=torch.float32, device=q.device)
@@ -274,12 +287,10 @@ def attn_bwd_noalloc(plan: Plan, q, k, v, o, do, lse, scale: Optional[float] = N
     import torch
 
     lib = load_library()
-    if do.stride() != o.stride():
-        raise LcaError("dO must have the layout of O", 1)
-    sh = _shape(q, k, v, o)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
+    sh = _shape(q, k, v, o, do, dq, dk, dv)
     st = lib.lca_attn_bwd_noalloc(plan.handle, ctypes.byref(sh), q.data_ptr(), k.data_ptr(),
                                   v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
                                   dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),

@@ -416,6 +416,23 @@ lca_status check_shape(const lca_plan* p, const lca_shape* s) {
 
 int64_t padded_seqlen(int seqlen) { return (static_cast<int64_t>(seqlen) + 127) / 128 * 128; }
 
+// Row strides of dO, dQ, dK, dV: 0 takes the matching input's (dO as O, dQ as Q, dK as
+// K, dV as V); each must cover its heads and be a multiple of 8 elements.
+struct GradStrides { int64_t dout, dq, dk, dv; };
+
+lca_status grad_strides(const lca_shape* s, GradStrides* g) {
+  g->dout = s->do_row_stride ? s->do_row_stride : s->o_row_stride;
+  g->dq = s->dq_row_stride ? s->dq_row_stride : s->q_row_stride;
+  g->dk = s->dk_row_stride ? s->dk_row_stride : s->k_row_stride;
+  g->dv = s->dv_row_stride ? s->dv_row_stride : s->v_row_stride;
+  const int64_t q_min = static_cast<int64_t>(s->h_q) * s->head_dim;
+  const int64_t k_min = static_cast<int64_t>(s->h_kv) * s->head_dim;
+  if (g->dout < q_min || g->dq < q_min || g->dk < k_min || g->dv < k_min)
+    return LCA_ERR_INVALID_ARG;
+  if ((g->dout | g->dq | g->dk | g->dv) & 7) return LCA_ERR_INVALID_ARG;
+  return LCA_OK;
+}
+
 AttnDims make_dims(const lca_plan* p, const lca_shape* s, float softmax_scale) {
   AttnDims d;
   d.batch = s->batch;
@@ -488,11 +505,14 @@ lca_status lca_attn_bwd(const lca_plan* plan, const lca_shape* shape, const void
   for (const void* ptr : ptrs)
     if (!aligned16(ptr)) return LCA_ERR_INVALID_ARG;
   if (ws_bytes < lca_attn_bwd_workspace(plan, shape, flags)) return LCA_ERR_INVALID_ARG;
+  GradStrides gs;
+  s = grad_strides(shape, &gs);
+  if (s != LCA_OK) return s;
   CUtensorMap tq, tk, tv, tdo;
   if (!make_tmap_bshd(&tq, q, shape->batch, shape->seqlen, shape->h_q, shape->q_row_stride, 128, shape->head_dim) ||
       !make_tmap_bshd(&tk, k, shape->batch, shape->seqlen, shape->h_kv, shape->k_row_stride, 128, shape->head_dim) ||
       !make_tmap_bshd(&tv, v, shape->batch, shape->seqlen, shape->h_kv, shape->v_row_stride, 128, shape->head_dim) ||
-      !make_tmap_bshd(&tdo, dout, shape->batch, shape->seqlen, shape->h_q, shape->o_row_stride, 128, shape->head_dim))
+      !make_tmap_bshd(&tdo, dout, shape->batch, shape->seqlen, shape->h_q, gs.dout, 128, shape->head_dim))
     return LCA_ERR_CUDA;
   BwdArgs a;
   a.dims = make_dims(plan, shape, softmax_scale);
@@ -508,7 +528,10 @@ lca_status lca_attn_bwd(const lca_plan* plan, const lca_shape* shape, const void
   a.dk = static_cast<__nv_bfloat16*>(dk);
   a.dv = static_cast<__nv_bfloat16*>(dv);
   a.o_row_stride = shape->o_row_stride;
-  a.k_row_stride = shape->k_row_stride;
+  a.do_row_stride = gs.dout;
+  a.dq_row_stride = gs.dq;
+  a.dk_row_stride = gs.dk;
+  a.dv_row_stride = gs.dv;
   a.err = device_error_ptr();
   a.timeout_ns = g_timeout_ns.load();
   if (!a.err) return LCA_ERR_CUDA;

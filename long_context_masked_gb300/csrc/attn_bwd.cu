@@ -60,8 +60,9 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(BwdArgs a) {
   float acc = 0.f;
   if (live) {
     const int64_t off = (b * S + i) * a.o_row_stride + h * HD + part * 8;
+    const int64_t goff = (b * S + i) * a.do_row_stride + h * HD + part * 8;
     const uint4 ov = *reinterpret_cast<const uint4*>(a.o + off);
-    const uint4 gv = *reinterpret_cast<const uint4*>(a.dout + off);
+    const uint4 gv = *reinterpret_cast<const uint4*>(a.dout + goff);
     const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
     const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gv);
 #pragma unroll
@@ -620,11 +621,13 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       __syncwarp();
       tc_fence_after();
     }
-    const int64_t roff = (static_cast<int64_t>(b) * S + j) * a.k_row_stride +
-                         static_cast<int64_t>(hk) * HD + half * ACOLS;
+    const int64_t col = static_cast<int64_t>(hk) * HD + half * ACOLS;
+    const int64_t pos = static_cast<int64_t>(b) * S + j;
     const uint32_t acc_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + half * ACOLS;
-    store_acc_half<ACOLS>(acc_addr + KV_TM_DV, t > 0, 1.f, a.dv + roff, jvalid);
-    store_acc_half<ACOLS>(acc_addr + KV_TM_DK, t > 0, dm.scale, a.dk + roff, jvalid);
+    store_acc_half<ACOLS>(acc_addr + KV_TM_DV, t > 0, 1.f, a.dv + pos * a.dv_row_stride + col,
+                          jvalid);
+    store_acc_half<ACOLS>(acc_addr + KV_TM_DK, t > 0, dm.scale,
+                          a.dk + pos * a.dk_row_stride + col, jvalid);
   }
 
   tc_fence_before();
@@ -893,14 +896,14 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     const int64_t rowi = (static_cast<int64_t>(b) * dm.h_q + h) * a.s_pad + i;
     const float lse2 = __ldg(a.lse2 + rowi);
     const float dsum = __ldg(a.dsum + rowi);
-    const int64_t roff = (static_cast<int64_t>(b) * S + i) * a.o_row_stride +
-                         static_cast<int64_t>(h) * HD + half * ACOLS;
+    const int64_t pos = static_cast<int64_t>(b) * S + i;
+    const int64_t col = static_cast<int64_t>(h) * HD + half * ACOLS;
     {
       // this thread's half row of dO (HD / 2 bf16) into TMEM columns
       // [DQ_TM_DO + DOC half, + DOC)
       uint32_t v[DOC];
       if (valid) {
-        const uint4* src = reinterpret_cast<const uint4*>(a.dout + roff);
+        const uint4* src = reinterpret_cast<const uint4*>(a.dout + pos * a.do_row_stride + col);
 #pragma unroll
         for (int u = 0; u < DOC / 4; ++u) {
           const uint4 w = __ldg(src + u);
@@ -965,7 +968,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       tc_fence_after();
     }
     store_acc_half<ACOLS>(quarter_addr + DQ_TM_DQ + half * ACOLS, n_tiles > 0, dm.scale,
-                          a.dq + roff, valid);
+                          a.dq + pos * a.dq_row_stride + col, valid);
   }
 
   tc_fence_before();

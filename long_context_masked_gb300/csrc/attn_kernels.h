@@ -34,8 +34,11 @@ struct BwdArgs {
   __nv_bfloat16* dq;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
-  int64_t o_row_stride;     // O, dO, dQ
-  int64_t k_row_stride;     // dK, dV
+  int64_t o_row_stride;     // O
+  int64_t do_row_stride;    // dO
+  int64_t dq_row_stride;    // dQ
+  int64_t dk_row_stride;    // dK
+  int64_t dv_row_stride;    // dV
   unsigned int* err;
   uint64_t timeout_ns;
 };

@@ -122,3 +122,28 @@ def test_python_constants_match_the_header():
         assert getattr(I, name) == vals[name], name
     for t, name in I.MASK_NAMES.items():
         assert vals[name] == t, name
+
+
+def test_shape_marshals_every_row_stride():
+    """The binding passes each tensor's own row stride: slices of a packed QKV tensor for
+    the inputs, separate buffers for the gradients (CPU tensors; no library call)."""
+    import torch
+
+    b, s, hq, hkv, d = 1, 10, 4, 2, 128
+    qkv = torch.zeros((b, s, hq + 2 * hkv, d), dtype=torch.bfloat16)
+    q, k, v = qkv[:, :, :hq], qkv[:, :, hq:hq + hkv], qkv[:, :, hq + hkv:]
+    o = torch.zeros((b, s, hq, d), dtype=torch.bfloat16)
+    do = torch.zeros((b, s, 2 * hq, d), dtype=torch.bfloat16)[:, :, hq:]
+    dq, dk, dv = torch.zeros_like(o), torch.zeros((b, s, hkv, d)).bfloat16(), \
+        torch.zeros((b, s, 3 * hkv, d), dtype=torch.bfloat16)[:, :, :hkv]
+    sh = binding._shape(q, k, v, o, do, dq, dk, dv)
+    packed = (hq + 2 * hkv) * d
+    assert (sh.q_row_stride, sh.k_row_stride, sh.v_row_stride) == (packed,) * 3
+    assert sh.o_row_stride == hq * d and sh.do_row_stride == 2 * hq * d
+    assert (sh.dq_row_stride, sh.dk_row_stride, sh.dv_row_stride) == (hq * d, hkv * d, 3 * hkv * d)
+    fwd = binding._shape(q, k, v, o)          # the forward leaves the gradient strides 0
+    assert (fwd.do_row_stride, fwd.dq_row_stride, fwd.dk_row_stride, fwd.dv_row_stride) == (0,) * 4
+    with pytest.raises(binding.LcaError):     # heads not packed at stride d
+        binding._shape(q, k, v, o, do, dq, dk, torch.zeros((b, s, hkv, 2 * d))[..., ::2])
+    with pytest.raises(binding.LcaError):     # wrong head count
+        binding._shape(q, k, v, o, do, dq, dk, torch.zeros((b, s, hkv + 1, d)))
