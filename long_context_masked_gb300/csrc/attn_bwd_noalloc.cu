@@ -8,6 +8,7 @@
 // out only the tensors of the op itself.  This entry point takes the workspace from a
 // fixed buffer compiled into the library instead, and otherwise runs exactly the
 // lca_attn_bwd path.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -24,21 +25,60 @@ constexpr size_t kScratchFloats = size_t(1) << 24;
 static __device__ __align__(256) float g_bwd_scratch[kScratchFloats];
 
 constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-float* g_scratch_ptr[kMaxDevices] = {};
 
-// Device address of g_bwd_scratch on the current device, looked up once per device.
-// In host code the symbol name is only a host-side handle, never a device address.
+// The device address of g_bwd_scratch, remembered per device together with the CUDA
+// context it was looked up in: a context torn down and re-created (cudaDeviceReset)
+// reloads the module, and the buffer may then sit at another address.
+struct ScratchAddr {
+  float* ptr = nullptr;
+  unsigned long long ctx_id = 0;   // 0: unknown, look the address up again
+};
+std::mutex g_mu;
+ScratchAddr g_scratch[kMaxDevices];
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+template <typename Fn>
+Fn driver_fn(const char* name) {
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  return reinterpret_cast<Fn>(p);
+}
+
+// Unique id of the calling thread's current context (false if there is none yet or the
+// driver does not report one).
+bool current_context_id(unsigned long long* id) {
+  static CtxGetCurrentFn get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+  static CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+  if (!get_current || !get_id) return false;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return false;
+  return get_id(ctx, id) == CUDA_SUCCESS && *id != 0;
+}
+
+// Device address of g_bwd_scratch on the current device.  In host code the symbol name
+// is only a host-side handle, never a device address, so the address is asked of the
+// runtime (with the device current) the first time and again whenever the context
+// changed.
 lca_status scratch_on_current_device(float** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return LCA_ERR_CUDA;
+  unsigned long long ctx = 0;
+  const bool known = current_context_id(&ctx);
   std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_scratch_ptr[dev]) {
+  ScratchAddr& e = g_scratch[dev];
+  if (!e.ptr || !known || e.ctx_id != ctx) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_bwd_scratch) != cudaSuccess || !p) return LCA_ERR_CUDA;
-    g_scratch_ptr[dev] = static_cast<float*>(p);
+    e.ptr = static_cast<float*>(p);
+    e.ctx_id = 0;
+    if (current_context_id(&ctx)) e.ctx_id = ctx;   // the lookup made the context current
   }
-  *out = g_scratch_ptr[dev];
+  *out = e.ptr;
   return LCA_OK;
 }
 

@@ -94,3 +94,51 @@ def small_descs(s, hq, hkv, seed=0):
         I.make_desc(I.BLOCK_SPARSE_VARIABLE, s, map_heads=hkv, map_seed=seed, cu_seqlens=cu),
     ]
     return out
+
+
+def oracle_bwd_heads(host, desc, heads, scale=None, workers=8):
+    """oracle.attn_bwd_ref over the given query heads, one head per worker thread (the
+    NumPy work releases the GIL), with dK/dV summed over the heads.  Returns the same
+    dict as attn_bwd_ref: dQ is filled for the given heads only, and dK/dV of a KV head
+    are complete when all of its query heads are given."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    import oracle
+
+    heads = list(heads)
+
+    def one(h):
+        return oracle.attn_bwd_ref(*host, desc, scale=scale, heads=[h])
+
+    with ThreadPoolExecutor(max(1, min(workers, len(heads)))) as ex:
+        parts = list(ex.map(one, heads))
+    out = parts[0]
+    for h, p in zip(heads[1:], parts[1:]):
+        out["dQ"][:, :, h] = p["dQ"][:, :, h]
+        out["O"][:, :, h] = p["O"][:, :, h]
+        out["LSE"][:, h] = p["LSE"][:, h]
+        out["D"][:, h] = p["D"][:, h]
+        out["dK"] += p["dK"]
+        out["dV"] += p["dV"]
+    return out
+
+
+def oracle_dkdv_cols(host, desc, kv_heads, cols, scale=None, workers=8):
+    """oracle.attn_dkdv_cols_ref with one KV head per worker thread."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    import oracle
+
+    def one(hk):
+        return oracle.attn_dkdv_cols_ref(*host, desc, kv_heads=[hk], cols=cols, scale=scale)
+
+    with ThreadPoolExecutor(max(1, min(workers, len(kv_heads)))) as ex:
+        parts = list(ex.map(one, list(kv_heads)))
+    return (np.concatenate([p[0] for p in parts]), np.concatenate([p[1] for p in parts]))
+
+
+def sampled_cols(s, n, seed):
+    """n sorted key positions: the first and last, the rest drawn without repetition."""
+    rng = np.random.default_rng(seed)
+    return np.sort(np.concatenate([rng.choice(np.arange(1, s - 1), n - 2, replace=False),
+                                   [0, s - 1]]))

@@ -6,7 +6,8 @@ import torch
 import long_context_masked_gb300 as lca
 import oracle
 from long_context_masked_gb300 import inputs as I
-from tests._gpu import check_grad, make_inputs, small_descs, to_np
+from tests._gpu import (check_grad, make_inputs, oracle_bwd_heads, oracle_dkdv_cols,
+                        sampled_cols, small_descs, to_np)
 
 pytestmark = pytest.mark.gpu
 
@@ -97,6 +98,37 @@ def test_one_kv_group_medium_in_full(mask, kw):
     _check_all(I.make_desc(mask, s, **kw), host, dev)
 
 
+@pytest.mark.parametrize("s,hq,hkv,mask,kw", [
+    (16384, 4, 2, I.CAUSAL, {}),
+    (16384, 4, 2, I.FULL_DOCUMENT, {"doc_seed": 11}),
+    (32768, 2, 2, I.GLOBAL_SLIDING, {"num_global": 256, "window": 4096}),
+    (16384, 16, 2, I.CAUSAL, {}),
+    (16384, 4, 2, I.BLOCK_CAUSAL_DOCUMENT, {"block": 1024, "doc_seed": 12}),
+])
+def test_multi_wave_grids_in_full(s, hq, hkv, mask, kw):
+    """dQ, dK and dV compared element by element with the full fp64 backward on grids of
+    several waves (256-512 dK/dV CTAs, 512-2048 dQ CTAs): the longest-first launch order,
+    the 16-item launch chunks and the group loops of the dK/dV kernel across waves.
+    16:2 at 16K runs one KV group of the 64:8 layout twice; BLOCK_CAUSAL_DOCUMENT takes
+    the pages' block of 1024."""
+    host, dev = make_inputs(1, s, hq, hkv, seed=700 + hq + mask)
+    desc = I.make_desc(mask, s, **kw)
+    _, _, grads = _run(desc, dev)
+    ref = oracle_bwd_heads(host, desc, range(hq))
+    for name, g in zip(("dQ", "dK", "dV"), grads):
+        check_grad(to_np(g), ref[name], f"{desc.name} {hq}:{hkv} S={s} {name}")
+
+
+def _sampled_dkdv(desc, host, grads, kv_heads, ncols, seed):
+    """dK/dV rows of sampled keys against the oracle's key-column backward, per KV head."""
+    s = host[0].shape[1]
+    cols = sampled_cols(s, ncols, seed)
+    rk, rv = oracle_dkdv_cols(host, desc, kv_heads, cols)
+    for a, hk in enumerate(kv_heads):
+        check_grad(to_np(grads[1][0, cols, hk]), rk[a], f"{desc.name} dK cols hk{hk}")
+        check_grad(to_np(grads[2][0, cols, hk]), rv[a], f"{desc.name} dV cols hk{hk}")
+
+
 def _invariants(desc, host, dev, grads, plan):
     """Properties that hold at any size: for every KV head, sum_j dK_j = 0 and
     sum_j dV_j = sum of dO over the group's non-empty rows (rows of P sum to 1)."""
@@ -136,6 +168,7 @@ def test_dense_regular_full_size(mask, kw):
     desc = I.make_desc(mask, s, **kw)
     plan, _, grads = _run(desc, dev)
     _sampled_dq(desc, host, grads, heads=[0, 17, 63], nrows=24, seed=mask)
+    _sampled_dkdv(desc, host, grads, kv_heads=[5], ncols=24, seed=mask)
     _invariants(desc, host, dev, grads, plan)
 
 
@@ -143,13 +176,16 @@ def test_dense_regular_full_size(mask, kw):
                                      (I.SHARED_QUESTION, {"question": 2048, "answers": [7680] * 4}),
                                      (I.GLOBAL_SLIDING, {"num_global": 256, "window": 4096}),
                                      (I.CAUSAL_BLOCKWISE, {"block": 2048}),
-                                     (I.BLOCK_CAUSAL_DOCUMENT, {"block": 2048, "doc_seed": 2})])
+                                     (I.BLOCK_CAUSAL_DOCUMENT, {"block": 2048, "doc_seed": 2}),
+                                     # the pages' block of 1024
+                                     (I.BLOCK_CAUSAL_DOCUMENT, {"block": 1024, "doc_seed": 3})])
 def test_heterogeneous_full_size(mask, kw):
     s = 32768
     host, dev = make_inputs(1, s, 64, 64, seed=400 + mask)
     desc = I.make_desc(mask, s, **kw)
     plan, _, grads = _run(desc, dev)
     _sampled_dq(desc, host, grads, heads=[0, 40], nrows=16, seed=mask)
+    _sampled_dkdv(desc, host, grads, kv_heads=[40], ncols=16, seed=mask)
     _invariants(desc, host, dev, grads, plan)
 
 
@@ -162,6 +198,8 @@ def test_uniform_block_sparse_full_size(s, block, hq, hkv, sparsity):
                        map_heads=map_heads, map_seed=block)
     plan, _, grads = _run(desc, dev)
     _sampled_dq(desc, host, grads, heads=[0, hq - 1], nrows=12, seed=block)
+    if s <= 32768:    # the key-column oracle evaluates every row that reaches a key
+        _sampled_dkdv(desc, host, grads, kv_heads=[hkv - 1], ncols=12, seed=block)
     _invariants(desc, host, dev, grads, plan)
 
 
@@ -171,6 +209,8 @@ def test_variable_block_sparse_long_varlen():
     desc = I.make_desc(I.BLOCK_SPARSE_VARIABLE, s, map_heads=8, map_seed=7, doc_seed=7)
     plan, _, grads = _run(desc, dev)
     _sampled_dq(desc, host, grads, heads=[0, 37], nrows=12, seed=7)
+    # documents keep the rows that reach a key few, so sampled keys are cheap here
+    _sampled_dkdv(desc, host, grads, kv_heads=[0, 4], ncols=32, seed=7)
     _invariants(desc, host, dev, grads, plan)
 
 

@@ -115,7 +115,9 @@ def test_dense_regular_full_size_sampled(mask, kw):
                                      (I.SHARED_QUESTION, {"question": 2048, "answers": [7680] * 4}),
                                      (I.GLOBAL_SLIDING, {"num_global": 256, "window": 4096}),
                                      (I.CAUSAL_BLOCKWISE, {"block": 2048}),
-                                     (I.BLOCK_CAUSAL_DOCUMENT, {"block": 2048, "doc_seed": 2})])
+                                     (I.BLOCK_CAUSAL_DOCUMENT, {"block": 2048, "doc_seed": 2}),
+                                     # the pages' block of 1024
+                                     (I.BLOCK_CAUSAL_DOCUMENT, {"block": 1024, "doc_seed": 3})])
 def test_heterogeneous_full_size_sampled(mask, kw):
     s = 32768
     desc = I.make_desc(mask, s, **kw)
