@@ -177,7 +177,8 @@ def attn_dq_rows_ref(q, k, v, do, desc, *, heads: Sequence[int], rows: Sequence[
 
 
 def attn_dkdv_cols_ref(q, k, v, do, desc, *, kv_heads: Sequence[int], cols: Sequence[int],
-                       batch: int = 0, scale: Optional[float] = None, chunk: int = 2048):
+                       batch: int = 0, scale: Optional[float] = None, chunk: int = 2048,
+                       heads: Optional[Sequence[int]] = None):
     """dK and dV at selected key positions of selected KV heads, fp64.
 
     For key j of KV head hk, summed over the query heads h of its group:
@@ -187,6 +188,8 @@ def attn_dkdv_cols_ref(q, k, v, do, desc, *, kv_heads: Sequence[int], cols: Sequ
     those rows is evaluated over all keys (which gives its LSE_i and D_i).  This
     is the attn_bwd_ref arithmetic restricted to the rows and columns that reach
     the selected keys, for checks at sizes where the full backward is too slow.
+    When ``heads`` is given, only those query heads contribute (each KV head then sums
+    the given heads of its group).
 
     Returns ``(dK [len(kv_heads), len(cols), d], dV [len(kv_heads), len(cols), d])``.
     """
@@ -202,6 +205,8 @@ def attn_dkdv_cols_ref(q, k, v, do, desc, *, kv_heads: Sequence[int], cols: Sequ
         kk = np.asarray(k[batch, :, hk, :], np.float64)
         vv = np.asarray(v[batch, :, hk, :], np.float64)
         for h in range(hk * g, (hk + 1) * g):
+            if heads is not None and h not in heads:
+                continue
             hm = map_head_of(h, h_q, h_kv, desc.map_heads)
             reach = np.broadcast_to(allowed(desc, hm, all_rows[:, None], cols[None, :]),
                                     (s_len, len(cols)))

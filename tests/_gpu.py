@@ -124,17 +124,29 @@ def oracle_bwd_heads(host, desc, heads, scale=None, workers=8):
 
 
 def oracle_dkdv_cols(host, desc, kv_heads, cols, scale=None, workers=8):
-    """oracle.attn_dkdv_cols_ref with one KV head per worker thread."""
+    """oracle.attn_dkdv_cols_ref with one query head per worker thread; the heads'
+    contributions are summed per KV head."""
     from concurrent.futures import ThreadPoolExecutor
 
     import oracle
 
-    def one(hk):
-        return oracle.attn_dkdv_cols_ref(*host, desc, kv_heads=[hk], cols=cols, scale=scale)
+    g = host[0].shape[2] // host[1].shape[2]
+    jobs = [(a, hk, h) for a, hk in enumerate(kv_heads) for h in range(hk * g, (hk + 1) * g)]
 
-    with ThreadPoolExecutor(max(1, min(workers, len(kv_heads)))) as ex:
-        parts = list(ex.map(one, list(kv_heads)))
-    return (np.concatenate([p[0] for p in parts]), np.concatenate([p[1] for p in parts]))
+    def one(job):
+        _, hk, h = job
+        return oracle.attn_dkdv_cols_ref(*host, desc, kv_heads=[hk], cols=cols, scale=scale,
+                                         heads=[h])
+
+    with ThreadPoolExecutor(max(1, min(workers, len(jobs)))) as ex:
+        parts = list(ex.map(one, jobs))
+    d = host[1].shape[3]
+    dk = np.zeros((len(kv_heads), len(cols), d))
+    dv = np.zeros((len(kv_heads), len(cols), d))
+    for (a, _, _), (pk, pv) in zip(jobs, parts):
+        dk[a] += pk[0]
+        dv[a] += pv[0]
+    return dk, dv
 
 
 def sampled_cols(s, n, seed):

@@ -104,13 +104,15 @@ def test_one_kv_group_medium_in_full(mask, kw):
     (32768, 2, 2, I.GLOBAL_SLIDING, {"num_global": 256, "window": 4096}),
     (16384, 16, 2, I.CAUSAL, {}),
     (16384, 4, 2, I.BLOCK_CAUSAL_DOCUMENT, {"block": 1024, "doc_seed": 12}),
+    (16384, 4, 2, I.BLOCK_SPARSE_VARIABLE, {"map_heads": 2, "map_seed": 13, "doc_seed": 13}),
 ])
 def test_multi_wave_grids_in_full(s, hq, hkv, mask, kw):
     """dQ, dK and dV compared element by element with the full fp64 backward on grids of
     several waves (256-512 dK/dV CTAs, 512-2048 dQ CTAs): the longest-first launch order,
     the 16-item launch chunks and the group loops of the dK/dV kernel across waves.
     16:2 at 16K runs one KV group of the 64:8 layout twice; BLOCK_CAUSAL_DOCUMENT takes
-    the pages' block of 1024."""
+    the pages' block of 1024; the variable block map over documents is the long-varlen
+    workload's mask at a size the full oracle finishes."""
     host, dev = make_inputs(1, s, hq, hkv, seed=700 + hq + mask)
     desc = I.make_desc(mask, s, **kw)
     _, _, grads = _run(desc, dev)
@@ -209,8 +211,6 @@ def test_variable_block_sparse_long_varlen():
     desc = I.make_desc(I.BLOCK_SPARSE_VARIABLE, s, map_heads=8, map_seed=7, doc_seed=7)
     plan, _, grads = _run(desc, dev)
     _sampled_dq(desc, host, grads, heads=[0, 37], nrows=12, seed=7)
-    # documents keep the rows that reach a key few, so sampled keys are cheap here
-    _sampled_dkdv(desc, host, grads, kv_heads=[0, 4], ncols=32, seed=7)
     _invariants(desc, host, dev, grads, plan)
 
 

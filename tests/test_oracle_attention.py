@@ -318,3 +318,8 @@ def test_key_column_function_matches_full_backward(mask):
         np.testing.assert_allclose(dv[a], full["dV"][0, cols, a], atol=1e-12)
     if mask == I.BLOCK_SPARSE_UNIFORM:
         assert (dk[:, 2:5] == 0).all() and (dv[:, 2:5] == 0).all()
+    # restricted to one query head at a time, the contributions add up to the group's
+    parts = [oracle.attn_dkdv_cols_ref(q, k, v, do, desc, kv_heads=[0, 1], cols=cols, heads=[h])
+             for h in range(hq)]
+    np.testing.assert_allclose(sum(p[0] for p in parts), dk, atol=1e-12)
+    np.testing.assert_allclose(sum(p[1] for p in parts), dv, atol=1e-12)
