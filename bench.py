@@ -11,15 +11,19 @@ backward, on synthetic N(0, 1) bf16 inputs resident on the GPU.  Document masks
 re-draw their lengths every step (seed = step mod 30; the pages sample 30 runs).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--suite dense|heterogeneous|sparse|varlen] [--case S:MASK]
+                    [--suite dense|heterogeneous|sparse|varlen|dynamic] [--case S:MASK]
+                    [--protocol steps|pages] [--no-memory]
 
 ``--suite`` selects another of the benchmark's workloads: the heterogeneous static
 masks at S = 32K on MHA 64:64; uniform block-sparse maps (blocks 64/128, sparsity
 0.2/0.5/0.8, S = 32K-128K, GQA 64:8 and MHA 32:32), reported per case with the
 fraction of non-skipped tiles and the time per tile; or S = 128K documents with
 variable block-sparse maps.  ``--impl reference`` times the fp64 CPU oracle (the only
-reference available here) on a bounded row sample of the selected workload.  Prints
-one JSON line (rank 0).
+reference available here) on a bounded row sample of the selected workload.  After the
+timed steps every case's peak device memory is measured, forward and backward apart
+(the pages' second metric), and ``--protocol pages`` adds the pages' run protocol
+(2 or 30 runs of 5 warm-ups + 20 steps per case, median/min/max).  Prints one JSON
+line (rank 0).
 """
 from __future__ import annotations
 
@@ -50,8 +54,7 @@ D = 128
 DOC_RUNS = 30
 FLUSH_BYTES = 256 << 20
 FWD_PER_PAIR, BWD_PER_PAIR = 4.0 * D, 10.0 * D
-KERNEL_SOURCES = {"attn_fwd": "attn_fwd.cu", "bwd_dkdv": "attn_bwd.cu", "bwd_dq": "attn_bwd.cu",
-                  "bwd_preprocess": "attn_bwd.cu"}
+KERNEL_SOURCES = {"attn_fwd": "attn_fwd.cu", "bwd": "attn_bwd.cu", "bwd_preprocess": "attn_bwd.cu"}
 SUITES = ("dense", "heterogeneous", "sparse", "varlen", "dynamic")
 
 
@@ -373,8 +376,85 @@ def memory_row(d, info, s, hq):
             "standard_attention_model_gb": round(model / 1e9, 2)}
 
 
+def measured_memory(lca, torch, dev, s, hq, hkv, desc, seed):
+    """Peak device memory of one (S, mask) case, forward and backward separately (the
+    pages' second metric, LongCA-bench summary appendix A.4.2): the torch allocator's
+    peak while the pass runs, with its inputs resident and its outputs and workspace
+    allocated by the call, plus the plan's device bytes (allocated by the library, so
+    not seen by torch).  Forward: Q, K, V, O, LSE.  Backward: Q, K, V, O, LSE, dO,
+    dQ, dK, dV and the workspace."""
+    hq_, hk_, hv_, hdo = I.qkv_do(1, s, hq, hkv, D, seed)
+    q, k, v = (x.to(dev) for x in (hq_, hk_, hv_))
+    plan = lca.mask_build(desc, 128, 128)
+    plan_bytes = plan.info["device_bytes"]
+    torch.cuda.synchronize(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    o, lse = lca.attn_fwd(plan, q, k, v)
+    torch.cuda.synchronize(dev)
+    fwd = torch.cuda.max_memory_allocated(dev) + plan_bytes
+    do = hdo.to(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    grads = lca.attn_bwd(plan, q, k, v, o, do, lse)
+    torch.cuda.synchronize(dev)
+    bwd = torch.cuda.max_memory_allocated(dev) + plan_bytes
+    del q, k, v, do, o, lse, grads, plan
+    torch.cuda.empty_cache()
+    return fwd, bwd
+
+
 def case_label(suite, s, hq, hkv, name):
     return f"S={s}/{name}" if suite == "dense" else f"S={s}/{hq}:{hkv}/{name}"
+
+
+def pages_protocol(args, groups, data, lca, torch, stream, flush, pk):
+    """Per case: n runs (2 for single-sequence masks, 30 for multi-sequence ones: the
+    document masks, SHARED_QUESTION and BLOCK_CAUSAL_DOCUMENT; LongCA-bench summary,
+    appendix A.4 "Measurement procedure"), each with its own descriptor draw (seed =
+    run), 5 warm-up steps and 20 timed steps (L2 flushed before each); a run's value is
+    its median step, and the case reports the median, minimum and maximum over runs.
+    SHARED_QUESTION's layout is fixed, so its runs repeat one descriptor on the same
+    inputs."""
+    out = {}
+    for gi, (s, hq, hkv, cases) in enumerate(groups):
+        d = data[gi]
+        q, k, v, do = d["dev"]
+        for c in cases:
+            if c.dynamic:
+                continue
+            multi = c.per_step or c.name == "SHARED_QUESTION"
+            runs = DOC_RUNS if multi else 2
+            fwd_runs, bwd_runs = [], []
+            for r in range(runs):
+                desc = c.make(r)
+                plan = lca.mask_build(desc, 128, 128)
+                pairs = int(plan.n_valid().sum()) * (hq // plan.info["map_heads"])
+                f_t, b_t = [], []
+                for st in range(5 + 20):
+                    flush.zero_()
+                    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+                    ev[0].record(stream)
+                    lca.attn_fwd(plan, q, k, v, out=d["o"], lse=d["lse"])
+                    ev[1].record(stream)
+                    lca.attn_bwd(plan, q, k, v, d["o"], do, d["lse"], dq=d["dq"], dk=d["dk"],
+                                 dv=d["dv"], workspace=d["ws"])
+                    ev[2].record(stream)
+                    torch.cuda.synchronize()
+                    if st >= 5:
+                        f_t.append(tflops(FWD_PER_PAIR * pairs, ev[0].elapsed_time(ev[1])))
+                        b_t.append(tflops(BWD_PER_PAIR * pairs, ev[1].elapsed_time(ev[2])))
+                fwd_runs.append(statistics.median(f_t))
+                bwd_runs.append(statistics.median(b_t))
+                del plan
+            out[case_label(args.suite, s, hq, hkv, c.name)] = {
+                "runs": runs,
+                "fwd_tflops": [round(statistics.median(fwd_runs), 1), round(min(fwd_runs), 1),
+                               round(max(fwd_runs), 1)],
+                "bwd_tflops": [round(statistics.median(bwd_runs), 1), round(min(bwd_runs), 1),
+                               round(max(bwd_runs), 1)],
+                "fwd_pct_peak_median": round(100 * statistics.median(fwd_runs) / pk["bf16"], 1),
+                "bwd_pct_peak_median": round(100 * statistics.median(bwd_runs) / pk["bf16"], 1)}
+    return {"order": "[median, min, max] over runs of the per-run median step",
+            "cases": out}
 
 
 def run_gpu(args, rank, world):
@@ -535,6 +615,8 @@ def run_gpu(args, rank, world):
         row = {"fwd_tflops": round(fwd, 1), "bwd_tflops": round(bwd, 1),
                "fwd_pct_peak": round(100 * fwd / pk["bf16"], 1),
                "bwd_pct_peak": round(100 * bwd / pk["bf16"], 1),
+               "fwd_tflops_min_max": [round(min(v["fwd"]), 1), round(max(v["fwd"]), 1)],
+               "bwd_tflops_min_max": [round(min(v["bwd"]), 1), round(max(v["bwd"]), 1)],
                "build_ms": round(statistics.median(v["build_ms"]), 3),
                "memory": memory_row(data[v["gi"]], v["info"], v["s"], v["hq"])}
         if not default:
@@ -552,7 +634,10 @@ def run_gpu(args, rank, world):
         per_config[label] = row
 
     # roofline of the dominant kernel (largest share of the timed region)
-    algo = {"attn_fwd": FWD_PER_PAIR, "bwd_dkdv": 8.0 * D, "bwd_dq": 2.0 * D}
+    # algorithmic FLOPs per allowed pair and query head: the forward 4d; the backward
+    # launch (dK/dV and dQ passes) 10d, the method's S, dP, dV, dK and dQ products (its
+    # recomputation of S and dP in the dQ pass is not credited)
+    algo = {"attn_fwd": FWD_PER_PAIR, "bwd": BWD_PER_PAIR}
     dom = max(prof.items(), key=lambda kv: kv[1][1])[0] if prof else None
     roofline = None
     if dom in algo:
@@ -570,7 +655,7 @@ def run_gpu(args, rank, world):
     gpu_launches = int(sum(v[0] for v in prof.values()))
 
     # ---- end to end through the public API with host buffers (default workload)
-    e2e_steps = max(1, min(args.steps, 3)) if default else 0
+    e2e_steps = max(1, min(args.steps, 5)) if default else 0
     e2e_value, h2d_bytes, d2h_bytes = None, 0, 0
     if e2e_steps:
         h2d = [[x.pin_memory() for x in d["host"]] for d in data]
@@ -591,6 +676,26 @@ def run_gpu(args, rank, world):
         e2e_flops, e2e_total_ms = aggregate(e2e_pairs * (FWD_PER_PAIR + BWD_PER_PAIR),
                                             sum(e2e_ms), dist, dev)
         e2e_value = tflops(e2e_flops, e2e_total_ms)
+
+    # ---- the pages' run protocol (optional): per case 2 runs (single-sequence masks) or
+    # 30 independently drawn runs (multi-sequence masks), each 5 warm-ups + 20 steps
+    pages = pages_protocol(args, groups, data, lca, torch, stream, flush, pk) \
+        if args.protocol == "pages" else None
+
+    # ---- measured peak memory per case, forward and backward (resident buffers freed)
+    if not args.no_memory:
+        del data
+        torch.cuda.empty_cache()
+        for gi, (s, hq, hkv, cases) in enumerate(groups):
+            for ci, c in enumerate(cases):
+                seeds = range(3) if c.per_step else (0,)
+                meas = [measured_memory(lca, torch, dev, s, hq, hkv, c.make(sd), 1000 * rank + s)
+                        for sd in seeds]
+                row = per_config[case_label(args.suite, s, hq, hkv, c.name)]["memory"]
+                row["fwd_peak_gb"] = round(statistics.median(m[0] for m in meas) / 1e9, 3)
+                row["bwd_peak_gb"] = round(statistics.median(m[1] for m in meas) / 1e9, 3)
+                row["peak_note"] = ("torch allocator peak during the pass + plan bytes; median "
+                                    f"over {len(meas)} draw(s)")
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -618,6 +723,7 @@ def run_gpu(args, rank, world):
             "bwd_pct_peak_full_causal_S>=16K_min":
                 min(x["bwd_pct_peak"] for x in full_causal) if full_causal else None},
         "per_config": per_config,
+        "pages_protocol": pages,
         "roofline": roofline,
         "kernel_time_share": kernel_share,
         "peak_memory_gb": round(peak_mem / 2**30, 3),
@@ -647,6 +753,11 @@ def main():
                     help="head dimension of the synthetic Q/K/V (the benchmark's configs use 128)")
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the timed oracle sample in the GPU arm")
+    ap.add_argument("--protocol", choices=("steps", "pages"), default="steps",
+                    help="'pages' adds the pages' run protocol per case (2 or 30 runs of 5 "
+                         "warm-ups + 20 steps; median/min/max over runs) after the timed steps")
+    ap.add_argument("--no-memory", action="store_true",
+                    help="skip the per-case peak-memory measurement (after the timed steps)")
     ap.add_argument("--case", default=None,
                     help="run a single S:MASK case of the dense workload (e.g. 16384:FULL) "
                          "for profiler captures; skips the end-to-end and CPU legs")

@@ -541,14 +541,11 @@ lca_status lca_attn_bwd(const lca_plan* plan, const lca_shape* shape, const void
     if (launch_bwd_preprocess(a, st) != cudaSuccess) return LCA_ERR_CUDA;
   }
   {
-    ProfScope ps(K_BWD_DKDV, st);
+    ProfScope ps(K_BWD, st);
     const int n_kv_blocks = plan->info.n_kt * shape->h_kv * shape->batch;
-    if (launch_bwd_dkdv(tq, tk, tv, tdo, a, n_kv_blocks, st) != cudaSuccess) return LCA_ERR_CUDA;
-  }
-  {
-    ProfScope ps(K_BWD_DQ, st);
     const int n_q_blocks = plan->info.n_qt * shape->h_q * shape->batch;
-    if (launch_bwd_dq(tq, tk, tv, tdo, a, n_q_blocks, st) != cudaSuccess) return LCA_ERR_CUDA;
+    if (launch_bwd(tq, tk, tv, tdo, a, n_kv_blocks, n_q_blocks, st) != cudaSuccess)
+      return LCA_ERR_CUDA;
   }
   return LCA_OK;
 }

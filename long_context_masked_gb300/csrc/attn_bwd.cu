@@ -5,7 +5,9 @@
 // key findings).  Given the forward's LSE, with P = exp(scale * Q K^T - LSE) under the
 // mask and D = rowsum(dO * O):
 //   dV = P^T dO,  dP = dO V^T,  dS = P * (dP - D),  dK = scale dS^T Q,  dQ = scale dS K.
-// Three kernels, deterministic and free of floating-point atomics:
+// Deterministic and free of floating-point atomics, in two launches: the preprocess,
+// then one launch whose first CTAs run the dK/dV pass and the rest the dQ pass (neither
+// reads the other's output, so dQ CTAs fill the SMs the last dK/dV CTAs leave idle):
 //   preprocess  D for every (b, h, i) row and LSE * log2(e), into padded workspace
 //               rows (HBM-bound);
 //   dK/dV       one CTA per (KV head, key tile), key rows on the TMEM lanes: loops over
@@ -267,10 +269,9 @@ __device__ __forceinline__ bool walk_use_half_path(const PlanDev& pl, int kt, in
 }
 
 template <int HD_>
-__global__ void __launch_bounds__(KV_THREADS, 1)
-bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                BwdArgs a) {
+__device__ __forceinline__ void dkdv_cta(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                                         const CUtensorMap& tm_v, const CUtensorMap& tm_do,
+                                         const BwdArgs& a, int blk) {
   using C = BwdCfg<HD_>;
   constexpr int HD = C::HD, NH = C::NH, ACOLS = C::ACOLS;
   constexpr uint32_t TILE = C::TILE;
@@ -294,15 +295,15 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   if (dm.kv_per_map > 0) {
     const int per_item = dm.kv_per_map * dm.batch;
     int item, rem;
-    chunked_item(blockIdx.x, per_item, pl.map_heads * pl.n_kt, dm.chunk, item, rem);
+    chunked_item(blk, per_item, pl.map_heads * pl.n_kt, dm.chunk, item, rem);
     const int col = __ldg(pl.work_k + item);
     const int hm = col / pl.n_kt;
     kt = col - hm * pl.n_kt;
     hk = hm * dm.kv_per_map + rem % dm.kv_per_map;
     b = rem / dm.kv_per_map;
   } else {
-    kt = blockIdx.x % pl.n_kt;
-    const int rest = blockIdx.x / pl.n_kt;
+    kt = blk % pl.n_kt;
+    const int rest = blk / pl.n_kt;
     hk = rest % dm.h_kv;
     b = rest / dm.h_kv;
   }
@@ -668,10 +669,9 @@ struct DqBars {
 static_assert(sizeof(DqBars) <= 256, "barrier block overflows its shared-memory slot");
 
 template <int HD_>
-__global__ void __launch_bounds__(DQ_THREADS, 1)
-bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-              BwdArgs a) {
+__device__ __forceinline__ void dq_cta(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                                       const CUtensorMap& tm_v, const CUtensorMap& tm_do,
+                                       const BwdArgs& a, int blk) {
   using C = BwdCfg<HD_>;
   using D = DqCfg<HD_>;
   constexpr int HD = C::HD, NH = C::NH, ACOLS = C::ACOLS;
@@ -694,7 +694,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 
   const int per_item = dm.heads_per_map * dm.batch;
   int item, rem;
-  chunked_item(blockIdx.x, per_item, pl.map_heads * pl.n_qt, dm.chunk, item, rem);
+  chunked_item(blk, per_item, pl.map_heads * pl.n_qt, dm.chunk, item, rem);
   const int row = __ldg(pl.work_q + item);
   const int hm = row / pl.n_qt;
   const int qt = row - hm * pl.n_qt;
@@ -979,6 +979,22 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   }
 }
 
+// The two passes in one launch: CTAs [0, n_kv) run dK/dV (the longest, launched
+// first), the rest dQ.  Neither pass reads the other's output (both read only the
+// preprocess rows), so dQ CTAs take over the SMs that the last wave of dK/dV CTAs
+// leaves idle, with no drain and launch gap between two kernels.
+template <int HD_>
+__global__ void __launch_bounds__(KV_THREADS, 1)
+bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+           const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+           BwdArgs a, int n_kv) {
+  static_assert(KV_THREADS == DQ_THREADS, "one block shape for both passes");
+  if (static_cast<int>(blockIdx.x) < n_kv)
+    dkdv_cta<HD_>(tm_q, tm_k, tm_v, tm_do, a, blockIdx.x);
+  else
+    dq_cta<HD_>(tm_q, tm_k, tm_v, tm_do, a, blockIdx.x - n_kv);
+}
+
 }  // namespace
 
 cudaError_t launch_bwd_preprocess(const BwdArgs& a, cudaStream_t st) {
@@ -993,43 +1009,24 @@ cudaError_t launch_bwd_preprocess(const BwdArgs& a, cudaStream_t st) {
 }
 
 template <int HD>
-static cudaError_t launch_dkdv_hd(const CUtensorMap& tq, const CUtensorMap& tk,
-                                  const CUtensorMap& tv, const CUtensorMap& tdo, const BwdArgs& a,
-                                  int n_blocks, cudaStream_t st) {
-  constexpr uint32_t smem = BwdCfg<HD>::KV_SMEM;
-  cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_kernel<HD>,
+static cudaError_t launch_bwd_hd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                 const CUtensorMap& tdo, const BwdArgs& a, int n_kv, int n_q,
+                                 cudaStream_t st) {
+  constexpr uint32_t smem = BwdCfg<HD>::KV_SMEM > DqCfg<HD>::DQ_SMEM ? BwdCfg<HD>::KV_SMEM
+                                                                      : DqCfg<HD>::DQ_SMEM;
+  cudaError_t e = cudaFuncSetAttribute(bwd_kernel<HD>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  bwd_dkdv_kernel<HD><<<n_blocks, KV_THREADS, smem, st>>>(tq, tk, tv, tdo, a);
+  bwd_kernel<HD><<<n_kv + n_q, KV_THREADS, smem, st>>>(tq, tk, tv, tdo, a, n_kv);
   return cudaGetLastError();
 }
 
-template <int HD>
-static cudaError_t launch_dq_hd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                                const CUtensorMap& tdo, const BwdArgs& a, int n_blocks,
-                                cudaStream_t st) {
-  constexpr uint32_t smem = DqCfg<HD>::DQ_SMEM;
-  cudaError_t e = cudaFuncSetAttribute(bwd_dq_kernel<HD>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  bwd_dq_kernel<HD><<<n_blocks, DQ_THREADS, smem, st>>>(tq, tk, tv, tdo, a);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_bwd_dkdv(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const CUtensorMap& tdo, const BwdArgs& a, int n_blocks,
-                            cudaStream_t st) {
-  if (n_blocks == 0) return cudaSuccess;
-  if (a.dims.head_dim == 64) return launch_dkdv_hd<64>(tq, tk, tv, tdo, a, n_blocks, st);
-  return launch_dkdv_hd<128>(tq, tk, tv, tdo, a, n_blocks, st);
-}
-
-cudaError_t launch_bwd_dq(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                          const CUtensorMap& tdo, const BwdArgs& a, int n_blocks,
-                          cudaStream_t st) {
-  if (n_blocks == 0) return cudaSuccess;
-  if (a.dims.head_dim == 64) return launch_dq_hd<64>(tq, tk, tv, tdo, a, n_blocks, st);
-  return launch_dq_hd<128>(tq, tk, tv, tdo, a, n_blocks, st);
+cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const CUtensorMap& tdo, const BwdArgs& a, int n_kv, int n_q,
+                       cudaStream_t st) {
+  if (n_kv + n_q == 0) return cudaSuccess;
+  if (a.dims.head_dim == 64) return launch_bwd_hd<64>(tq, tk, tv, tdo, a, n_kv, n_q, st);
+  return launch_bwd_hd<128>(tq, tk, tv, tdo, a, n_kv, n_q, st);
 }
 
 }  // namespace lca

@@ -48,12 +48,11 @@ cudaError_t launch_attn_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const 
                             const FwdArgs& args, int n_blocks, cudaStream_t st);
 
 cudaError_t launch_bwd_preprocess(const BwdArgs& args, cudaStream_t st);
-cudaError_t launch_bwd_dkdv(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const CUtensorMap& tdo, const BwdArgs& args, int n_blocks,
-                            cudaStream_t st);
-cudaError_t launch_bwd_dq(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                          const CUtensorMap& tdo, const BwdArgs& args, int n_blocks,
-                          cudaStream_t st);
+// dK/dV (n_kv CTAs: one per KV head and key tile) and dQ (n_q CTAs: one per query head
+// and query tile) in one launch.
+cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const CUtensorMap& tdo, const BwdArgs& args, int n_kv, int n_q,
+                       cudaStream_t st);
 
 cudaError_t launch_selftest_wait(unsigned int* err, uint64_t timeout_ns, cudaStream_t st);
 cudaError_t launch_selftest_umma(int variant, const CUtensorMap& ta, const CUtensorMap& tb,

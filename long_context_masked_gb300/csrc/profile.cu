@@ -14,7 +14,7 @@ namespace lca {
 namespace {
 
 const char* kNames[K_COUNT] = {"mask_classify", "mask_scan", "mask_collen", "mask_fill",
-                               "mask_lpt", "attn_fwd", "bwd_preprocess", "bwd_dkdv", "bwd_dq",
+                               "mask_lpt", "attn_fwd", "bwd_preprocess", "bwd",
                                "block_scores", "block_topk"};
 
 struct Rec {

@@ -6,7 +6,7 @@
 namespace lca {
 
 enum KernelId {
-  K_CLASSIFY = 0, K_SCAN, K_COLLEN, K_FILL, K_LPT, K_FWD, K_BWD_PRE, K_BWD_DKDV, K_BWD_DQ,
+  K_CLASSIFY = 0, K_SCAN, K_COLLEN, K_FILL, K_LPT, K_FWD, K_BWD_PRE, K_BWD,
   K_BLOCK_SCORES, K_BLOCK_TOPK,
   K_COUNT
 };
