@@ -684,7 +684,7 @@ def run_gpu(args, rank, world):
 
     # ---- measured peak memory per case, forward and backward (resident buffers freed)
     if not args.no_memory:
-        del data
+        del data, flush
         torch.cuda.empty_cache()
         for gi, (s, hq, hkv, cases) in enumerate(groups):
             for ci, c in enumerate(cases):
