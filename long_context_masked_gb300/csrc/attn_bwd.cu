@@ -502,11 +502,14 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tm_q, const CUtensor
           mbar_wait(&bar.do_full[0], 0, wc);
           issue_dp(0, eh);
         }
+        // Issue order dV(t), S^T(t+1), dK(t), dP^T(t+1): S^T(t+1) runs while the softmax
+        // still turns dP^T(t) into dS^T(t).  S^T(t+1) overwrites P^T(t) and dP^T(t+1)
+        // overwrites dS^T(t); tcgen05 MMAs of one thread run in issue order, so dV(t)
+        // (dK(t)) has read them by then.
         for (int t = 0; t < total && !bar.abort; ++t) {
+          const int eh_t = eh;
           mbar_wait(&bar.p_ready, t & 1, wc);
-          issue_dv(t, eh);
-          mbar_wait(&bar.ds_ready, t & 1, wc);
-          issue_dk(t, eh);
+          issue_dv(t, eh_t);
           const int n = t + 1;
           if (n < total) {
             if constexpr (HALVES) {
@@ -514,10 +517,12 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tm_q, const CUtensor
               fetch();
             }
             mbar_wait(&bar.q_full[n % KV_QST], (n / KV_QST) & 1, wc);
-            mbar_wait(&bar.dv_done, t & 1, wc);      // P^T(t) consumed
             issue_s(n, eh);
+          }
+          mbar_wait(&bar.ds_ready, t & 1, wc);
+          issue_dk(t, eh_t);
+          if (n < total) {
             mbar_wait(&bar.do_full[n % KV_DOST], (n / KV_DOST) & 1, wc);
-            mbar_wait(&bar.dk_done, t & 1, wc);      // dS^T(t) consumed
             issue_dp(n, eh);
           }
         }
