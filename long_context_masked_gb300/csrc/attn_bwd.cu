@@ -648,9 +648,9 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tm_q, const CUtensor
 
 // dO only ever feeds dP = dO V^T as the A operand, so it sits in TMEM (bf16 pairs, 64
 // columns, stored once per CTA by the softmax threads) and dP is a TS MMA; the shared
-// memory it frees gives K (held from S to dQ) a fourth stage.
-constexpr int DQ_KST = 4;                        // K stages (K is held until the dQ MMA)
-constexpr int DQ_VST = 2;                        // V stages (V is released after dP)
+// memory it frees gives the K and V rings three stages each.
+constexpr int DQ_KST = 3;                        // K stages (K is held until the dQ MMA)
+constexpr int DQ_VST = 3;                        // V stages (V is released after dP)
 
 template <int HD_>
 struct DqCfg {
