@@ -476,6 +476,8 @@ def run_gpu(args, rank, world):
     groups, text = workload(args.suite, args.case)
     default = args.suite == "dense" and not args.case
     tag = "bench_default" if default else (f"case_{args.case}" if args.case else args.suite)
+    if D != 128:
+        tag += f"_d{D}"     # profiles/ record traffic per head dimension
 
     # resident inputs (one batch entry per GPU, seeded by rank) and output buffers
     data = []
@@ -601,14 +603,22 @@ def run_gpu(args, rank, world):
         w_ms = ev[2].elapsed_time(ev[3])
         acc = per_cfg.setdefault(case_label(args.suite, s, hq, hkv, name),
                                  {"fwd": [], "bwd": [], "build_ms": [], "fwd_ms": [],
-                                  "bwd_ms": [], "pairs": [], "info": info, "hq": hq, "gi": gi,
-                                  "s": s})
+                                  "bwd_ms": [], "pairs": [], "eff": [], "f_tile_us": [],
+                                  "b_tile_us": [], "nonskip": [], "info": info, "hq": hq,
+                                  "gi": gi, "s": s})
         acc["fwd"].append(tflops(FWD_PER_PAIR * hp, f_ms))
         acc["bwd"].append(tflops(BWD_PER_PAIR * hp, w_ms))
         acc["build_ms"].append(b_ms)
         acc["fwd_ms"].append(f_ms)
         acc["bwd_ms"].append(w_ms)
         acc["pairs"].append(hp)
+        # allowed pairs per pair of this step's non-skipped head-tiles (re-drawn masks
+        # change both from step to step)
+        head_tiles = info["nnz"] * (hq // info["map_heads"])
+        acc["eff"].append(hp / (head_tiles * 128 * 128))
+        acc["f_tile_us"].append(1e3 * f_ms / head_tiles)
+        acc["nonskip"].append(info["nnz"] / (info["map_heads"] * info["n_qt"] * info["n_kt"]))
+        acc["b_tile_us"].append(1e3 * w_ms / head_tiles)
     per_config = {}
     for label, v in per_cfg.items():
         fwd, bwd = statistics.median(v["fwd"]), statistics.median(v["bwd"])
@@ -620,17 +630,13 @@ def run_gpu(args, rank, world):
                "build_ms": round(statistics.median(v["build_ms"]), 3),
                "memory": memory_row(data[v["gi"]], v["info"], v["s"], v["hq"])}
         if not default:
-            inf = v["info"]
-            head_tiles = inf["nnz"] * (v["hq"] // inf["map_heads"])
             f_ms, w_ms = statistics.median(v["fwd_ms"]), statistics.median(v["bwd_ms"])
             row.update({"fwd_ms": round(f_ms, 3), "bwd_ms": round(w_ms, 3),
-                        "nonskipped_tile_fraction":
-                            round(inf["nnz"] / (inf["map_heads"] * inf["n_qt"] * inf["n_kt"]), 4),
+                        "nonskipped_tile_fraction": round(statistics.median(v["nonskip"]), 4),
                         # allowed pairs per pair of the non-skipped tiles (partial-tile waste)
-                        "tile_efficiency": round(statistics.median(v["pairs"]) /
-                                                 (head_tiles * 128 * 128), 4),
-                        "fwd_us_per_head_tile": round(1e3 * f_ms / head_tiles, 4),
-                        "bwd_us_per_head_tile": round(1e3 * w_ms / head_tiles, 4)})
+                        "tile_efficiency": round(statistics.median(v["eff"]), 4),
+                        "fwd_us_per_head_tile": round(statistics.median(v["f_tile_us"]), 4),
+                        "bwd_us_per_head_tile": round(statistics.median(v["b_tile_us"]), 4)})
         per_config[label] = row
 
     # roofline of the dominant kernel (largest share of the timed region)
