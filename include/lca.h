@@ -196,7 +196,10 @@ void lca_plan_destroy(lca_plan* plan);
  * returns LCA_ERR_UNSUPPORTED (the attention kernels run 128 x 128 tiles only, and
  * leave out the empty 64-row / 64-column halves of a tile instead: see the tile-byte
  * flags above).  Reads q/k/v/o_row_stride only.  softmax_scale <= 0 means
- * 1/sqrt(head_dim). */
+ * 1/sqrt(head_dim).  The launch runs one persistent CTA per SM that takes (query tile,
+ * head) units from a counter the plan owns; each call takes the next of the plan's 16
+ * counters (and zeroes it first on `stream`), so at most 16 forward calls that share a
+ * plan may be in flight on the GPU at once. */
 lca_status lca_attn_fwd(const lca_plan* plan, const lca_shape* shape, const void* q,
                         const void* k, const void* v, void* o, float* lse, float softmax_scale,
                         void* stream);

@@ -73,6 +73,14 @@ bool make_tmap_bshd(CUtensorMap* m, const void* ptr, int batch, int seqlen, int 
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// SMs of the current device (the persistent forward runs one CTA per SM).
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+  return n;
+}
+
 bool is_sparse_type(int t) { return t == LCA_BLOCK_SPARSE_UNIFORM || t == LCA_BLOCK_SPARSE_VARIABLE; }
 
 bool needs_segments(int t) {
@@ -156,11 +164,17 @@ lca_status validate_desc(const lca_mask_desc* d, int tile_q, int tile_k) {
 
 }  // namespace
 
+// Unit counters of the forward's persistent CTAs: a launch takes the next of
+// kFwdCounters counters, so up to that many forward launches of one plan may overlap.
+constexpr int kFwdCounters = 16;
+
 struct lca_plan {
   lca_plan_info info{};
   MaskDev mask{};
   PlanDev dev{};
   unsigned long long* n_valid = nullptr;
+  unsigned int* fwd_counters = nullptr;   // [kFwdCounters]
+  std::atomic<unsigned int> fwd_next{0};
   std::vector<void*> allocs;
   size_t bytes = 0;   // device memory held by the plan
 
@@ -275,7 +289,9 @@ lca_status lca_mask_build(const lca_mask_desc* desc, int tile_q, int tile_k, voi
   int32_t* work_q = p->alloc<int32_t>(n_rows);
   int32_t* work_k = p->alloc<int32_t>(n_cols);
   unsigned long long* counters = p->alloc<unsigned long long>(hm_n + 1);
-  if (!cls || !rowlen || !rowptr || !collen || !colptr || !work_q || !work_k || !counters)
+  p->fwd_counters = p->alloc<unsigned int>(kFwdCounters);
+  if (!cls || !rowlen || !rowptr || !collen || !colptr || !work_q || !work_k || !counters ||
+      !p->fwd_counters)
     return fail(LCA_ERR_OOM);
   p->n_valid = counters;
   if (!cuda_ok(cudaMemsetAsync(counters, 0, (hm_n + 1) * sizeof(unsigned long long), st)))
@@ -478,10 +494,15 @@ lca_status lca_attn_fwd(const lca_plan* plan, const lca_shape* shape, const void
   a.err = device_error_ptr();
   a.timeout_ns = g_timeout_ns.load();
   if (!a.err) return LCA_ERR_CUDA;
-  const int n_blocks = plan->info.n_qt * shape->h_q * shape->batch;
+  a.n_units = plan->info.n_qt * shape->h_q * shape->batch;
+  lca_plan* mp = const_cast<lca_plan*>(plan);
+  a.unit_counter = mp->fwd_counters + (mp->fwd_next.fetch_add(1) % kFwdCounters);
+  const int sms = sm_count();
+  if (sms <= 0) return LCA_ERR_CUDA;
+  const int n_ctas = a.n_units < sms ? a.n_units : sms;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   ProfScope ps(K_FWD, st);
-  return launch_attn_fwd(tq, tk, tv, a, n_blocks, st) == cudaSuccess ? LCA_OK : LCA_ERR_CUDA;
+  return launch_attn_fwd(tq, tk, tv, a, n_ctas, st) == cudaSuccess ? LCA_OK : LCA_ERR_CUDA;
 }
 
 size_t lca_attn_bwd_workspace(const lca_plan* plan, const lca_shape* shape, int flags) {

@@ -4,21 +4,31 @@
 // the LongCA-bench kernels are measured on ("Long-Context Attention Benchmark":
 // summary page, abstract and sections 2.2 / 3.1; reading note, "Key design" 2).
 //
-// One CTA owns one 128-row query tile of one query head and walks that tile's list
-// of non-skipped key tiles (from the tile plan, longest lists launched first):
-//   warps 8, 10 TMA producers: Q once and the K tiles (warp 8), the V tiles (warp 10),
-//               each into a 3-stage ring;
+// Persistent CTAs, at most one per SM, work through units (one 128-row query tile of
+// one query head and batch entry, with the tile's list of non-skipped key tiles from
+// the tile plan).  Units are handed out in longest-first order by a global counter: the
+// K producer thread takes the next unit when it starts loading that unit's K tiles and
+// passes it to the other roles through a ring of shared-memory slots, so an SM moves on
+// to its next unit without a CTA exit, launch and prologue, and the next unit's loads
+// and first S MMAs overlap the end of the current one.  Roles:
+//   warp 8      unit fetcher and K producer: the K tiles of every unit into a 3-stage
+//               ring (the ring and every barrier phase follow one tile counter across
+//               units), the next unit's Q prefetched into L2;
+//   warp 10     Q and V producer: a unit's Q once the previous unit's last S has read
+//               the Q buffer, then its V tiles into a 3-stage ring;
 //   warp 9      TMEM owner and MMA issuer: S_n = Q K_n^T (tcgen05, both operands in
 //               shared memory, fp32 in TMEM, three buffers) and O += P_{n-2} V_{n-2}
 //               with P read from TMEM (accumulated in TMEM).  PV trails S by two
-//               tiles so that S_{n+1} is computed while the softmax works on S_n;
+//               tiles so that S_{n+1} is computed while the softmax works on S_n.  A
+//               unit's first PV (which overwrites O) waits until the softmax warps have
+//               read the previous unit's O; its first two S MMAs do not;
 //   warps 0-7   softmax, two threads per query row (warps w and w+4 share TMEM lanes
 //               and take key columns 0-63 / 64-127): read S_n from TMEM, apply the mask
 //               bits only on partial or ragged tiles, combine the two halves' row
 //               maxima through shared memory, online softmax in fp32 with exp2, write P
 //               (bf16 pairs) back into the TMEM columns of S_n for the PV MMA, rescale
 //               the O accumulator in TMEM when the running max moves by more than 2^8
-//               (exact after the final 1/l normalisation), then the epilogue.
+//               (exact after the final 1/l normalisation), then the unit's epilogue.
 // In a row of at least 64 plan entries of which at least a quarter flag one key half of
 // their tile as empty (no allowed pair: block maps on a grid finer than the tile, ragged tails),
 // such a tile runs at half width: S is an N = 64 MMA on the other half's keys, PV takes
@@ -66,7 +76,7 @@ struct Cfg {
   static constexpr uint32_t OFF_K = OFF_Q + TILE_BYTES;       // KST stages
   static constexpr uint32_t OFF_V = OFF_K + KST * TILE_BYTES; // VST stages
   static constexpr uint32_t OFF_BAR = OFF_V + VST * TILE_BYTES;
-  static constexpr uint32_t OFF_RED = OFF_BAR + 256;          // row-max / row-sum exchange
+  static constexpr uint32_t OFF_RED = OFF_BAR + 320;          // row-max / row-sum exchange
   static constexpr uint32_t SMEM_BYTES = OFF_RED + 2 * 2 * BM * 4;
   static constexpr int OCOLS = HD / 2;                        // O columns per softmax thread
   static_assert(HD == 64 || HD == 128, "head_dim 64 or 128");
@@ -87,15 +97,20 @@ __device__ __forceinline__ void tmem_stn(uint32_t taddr, const uint32_t (&r)[N])
   if constexpr (N == 64) tmem_st64(taddr, r); else tmem_st32(taddr, r);
 }
 
+constexpr int UR = 4;                 // unit ring slots
+constexpr int UNIT_READERS = 10;      // V producer, MMA warp, eight softmax warps
+
 struct Bars {
-  uint64_t q_full;
+  uint64_t q_full, q_empty, o_free;
+  uint64_t unit_full[UR], unit_empty[UR];
   uint64_t k_full[KST], k_empty[KST];
   uint64_t v_full[VST], v_empty[VST];
   uint64_t s_full[NSB], p_ready[NSB], pv_done[NSB];
   uint32_t tmem_base;
   int abort;
+  int unit[UR];
 };
-static_assert(sizeof(Bars) <= 256, "barrier block overflows its shared-memory slot");
+static_assert(sizeof(Bars) <= 320, "barrier block overflows its shared-memory slot");
 
 __device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, int kk) {
   return desc_kmajor(tile, kk, HALF_BYTES);
@@ -125,26 +140,40 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-
-  // ---- work item
   const AttnDims& dm = a.dims;
   const PlanDev& pl = a.plan;
-  const int per_item = dm.heads_per_map * dm.batch;
-  int item, rem;
-  chunked_item(blockIdx.x, per_item, pl.map_heads * pl.n_qt, dm.chunk, item, rem);
-  const int sub = rem % dm.heads_per_map;
-  const int b = rem / dm.heads_per_map;
-  const int row = __ldg(pl.work_q + item);
-  const int hm = row / pl.n_qt;
-  const int qt = row - hm * pl.n_qt;
-  const int h = hm * dm.heads_per_map + sub;
-  const int hk = h / dm.group;
-  const int beg = __ldg(pl.rowptr + row);
-  const int n_tiles = __ldg(pl.rowptr + row + 1) - beg;
   const int S = dm.seqlen;
+  const int n_units = a.n_units;
+
+  // A unit is one (query tile, query head, batch entry).  Units are handed out in
+  // longest-first order by a global counter: one thread (the K producer) takes the next
+  // unit when it starts loading that unit's K tiles and passes it to the other roles
+  // through a ring of UR shared-memory slots.
+  struct Unit { int h, hk, hm, qt, b, beg, n; };
+  auto decode = [&](int u) {
+    const int per_item = dm.heads_per_map * dm.batch;
+    int item, rem;
+    chunked_item(u, per_item, pl.map_heads * pl.n_qt, dm.chunk, item, rem);
+    Unit w;
+    const int row = __ldg(pl.work_q + item);
+    w.hm = row / pl.n_qt;
+    w.qt = row - w.hm * pl.n_qt;
+    w.h = w.hm * dm.heads_per_map + rem % dm.heads_per_map;
+    w.b = rem / dm.heads_per_map;
+    w.hk = w.h / dm.group;
+    w.beg = __ldg(pl.rowptr + row);
+    w.n = __ldg(pl.rowptr + row + 1) - w.beg;
+    return w;
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(&bar.q_full, 1);
+    mbar_init(&bar.q_empty, 1);
+    mbar_init(&bar.o_free, SOFTMAX_THREADS);
+    for (int s = 0; s < UR; ++s) {
+      mbar_init(&bar.unit_full[s], 1);
+      mbar_init(&bar.unit_empty[s], UNIT_READERS);
+    }
     for (int s = 0; s < KST; ++s) {
       mbar_init(&bar.k_full[s], 1);
       mbar_init(&bar.k_empty[s], 1);
@@ -171,296 +200,370 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   const uint32_t tmem = bar.tmem_base;
   WaitCtx wc{&bar.abort, a.err, a.timeout_ns};
 
-  if (warp == WARP_PRODUCER || warp == WARP_PRODUCER_V) {
-    // ------------------------------------------------ TMA producers
-    // one warp streams Q and the K tiles, another the V tiles, so a K load never
-    // queues behind the release of a V stage (V stages are freed two tiles later).
-    if (warp == WARP_PRODUCER && lane == 0) {
-      tma_prefetch_desc(&tm_q);
+  // The k-th unit of this CTA sits in ring slot k % UR.  Readers other than the fetcher:
+  // the V producer, the MMA warp and the eight softmax warps (lane 0 of each arrives once
+  // its warp has read the slot).  A unit index >= n_units ends every role's loop.
+  // WHOLE: called by all 32 lanes of a warp (lane 0 arrives after the warp has read the
+  // slot); otherwise by one lane alone, which arrives itself.
+  auto take_unit = [&](int k, bool whole) {
+    const int slot = k % UR;
+    mbar_wait(&bar.unit_full[slot], (k / UR) & 1, wc);
+    const int u = bar.abort ? n_units : bar.unit[slot];
+    if (whole) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar.unit_empty[slot]);
+    } else {
+      mbar_arrive(&bar.unit_empty[slot]);
+    }
+    return u;
+  };
+
+  // The K/V rings, the S buffers and every barrier phase follow one tile counter g across
+  // units; every role walks the same unit sequence, so the counters agree.
+  if (warp == WARP_PRODUCER) {
+    // ------------------------------------------------ unit fetcher and K producer
+    if (lane == 0) {
       tma_prefetch_desc(&tm_k);
-      mbar_arrive_expect_tx(&bar.q_full, TILE_BYTES);
-      for (int c = 0; c < C::NH; ++c)
-        tma_load_4d(base + OFF_Q + c * HALF_BYTES, &tm_q, &bar.q_full, c * 64, h, qt * BM, b);
-      for (int n = 0; n < n_tiles; ++n) {
-        const int kt = __ldg(pl.kt_idx + beg + n);
-        const int ks = n % KST;
-        if (n + KST < n_tiles) {   // L2 prefetch one ring ahead
-          const int ka = __ldg(pl.kt_idx + beg + n + KST);
-          for (int c = 0; c < C::NH; ++c) tma_prefetch_l2_4d(&tm_k, c * 64, hk, ka * BN, b);
+      tma_prefetch_desc(&tm_q);
+      int g = 0;
+      for (int k = 0;; ++k) {
+        const int slot = k % UR;
+        if (k >= UR) mbar_wait(&bar.unit_empty[slot], (k / UR - 1) & 1, wc);
+        const int u = bar.abort ? n_units : static_cast<int>(atomicAdd(a.unit_counter, 1u));
+        bar.unit[slot] = u;
+        mbar_arrive(&bar.unit_full[slot]);
+        if (u >= n_units) break;
+        const Unit w = decode(u);
+        // the unit's Q is loaded only after the previous unit's last S; prefetching it into
+        // L2 now (this thread runs a few tiles ahead) shortens that load
+        if (w.n > 0)
+          for (int c = 0; c < C::NH; ++c) tma_prefetch_l2_4d(&tm_q, c * 64, w.h, w.qt * BM, w.b);
+        for (int n = 0; n < w.n; ++n, ++g) {
+          const int kt = __ldg(pl.kt_idx + w.beg + n);
+          const int ks = g % KST;
+          if (n + KST < w.n) {   // L2 prefetch one ring ahead
+            const int ka = __ldg(pl.kt_idx + w.beg + n + KST);
+            for (int c = 0; c < C::NH; ++c) tma_prefetch_l2_4d(&tm_k, c * 64, w.hk, ka * BN, w.b);
+          }
+          if (g >= KST) mbar_wait(&bar.k_empty[ks], (g / KST - 1) & 1, wc);
+          mbar_arrive_expect_tx(&bar.k_full[ks], TILE_BYTES);
+          for (int c = 0; c < C::NH; ++c)
+            tma_load_4d(base + OFF_K + ks * TILE_BYTES + c * HALF_BYTES, &tm_k, &bar.k_full[ks],
+                        c * 64, w.hk, kt * BN, w.b);
         }
-        if (n >= KST) mbar_wait(&bar.k_empty[ks], (n / KST - 1) & 1, wc);
-        mbar_arrive_expect_tx(&bar.k_full[ks], TILE_BYTES);
-        for (int c = 0; c < C::NH; ++c)
-          tma_load_4d(base + OFF_K + ks * TILE_BYTES + c * HALF_BYTES, &tm_k, &bar.k_full[ks],
-                      c * 64, hk, kt * BN, b);
       }
       if (bar.abort) {  // let copies in flight land before the CTA exits
-        mbar_wait_final(&bar.q_full, 0, a.timeout_ns);
-        for (int n = max(0, n_tiles - KST); n < n_tiles; ++n)
+        for (int n = max(0, g - KST); n < g; ++n)
           mbar_wait_final(&bar.k_full[n % KST], (n / KST) & 1, a.timeout_ns);
       }
-    } else if (warp == WARP_PRODUCER_V && lane == 0) {
+    }
+  } else if (warp == WARP_PRODUCER_V) {
+    // ------------------------------------------------ Q and V producer
+    // A unit's Q is loaded once the previous unit's last S MMA has read its Q (q_empty).
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_v);
-      for (int n = 0; n < n_tiles; ++n) {
-        const int kt = __ldg(pl.kt_idx + beg + n);
-        const int vs = n % VST;
-        if (n + VST < n_tiles) {
-          const int ka = __ldg(pl.kt_idx + beg + n + VST);
-          for (int c = 0; c < C::NH; ++c) tma_prefetch_l2_4d(&tm_v, c * 64, hk, ka * BN, b);
-        }
-        if (n >= VST) mbar_wait(&bar.v_empty[vs], (n / VST - 1) & 1, wc);
-        mbar_arrive_expect_tx(&bar.v_full[vs], TILE_BYTES);
+      int g = 0, nq = 0;
+      for (int k = 0;; ++k) {
+        const int u = take_unit(k, false);
+        if (u >= n_units) break;
+        const Unit w = decode(u);
+        if (w.n == 0) continue;
+        if (nq > 0) mbar_wait(&bar.q_empty, (nq - 1) & 1, wc);
+        mbar_arrive_expect_tx(&bar.q_full, TILE_BYTES);
         for (int c = 0; c < C::NH; ++c)
-          tma_load_4d(base + OFF_V + vs * TILE_BYTES + c * HALF_BYTES, &tm_v, &bar.v_full[vs],
-                      c * 64, hk, kt * BN, b);
+          tma_load_4d(base + OFF_Q + c * HALF_BYTES, &tm_q, &bar.q_full, c * 64, w.h, w.qt * BM,
+                      w.b);
+        ++nq;
+        for (int n = 0; n < w.n; ++n, ++g) {
+          const int kt = __ldg(pl.kt_idx + w.beg + n);
+          const int vs = g % VST;
+          if (n + VST < w.n) {
+            const int ka = __ldg(pl.kt_idx + w.beg + n + VST);
+            for (int c = 0; c < C::NH; ++c) tma_prefetch_l2_4d(&tm_v, c * 64, w.hk, ka * BN, w.b);
+          }
+          if (g >= VST) mbar_wait(&bar.v_empty[vs], (g / VST - 1) & 1, wc);
+          mbar_arrive_expect_tx(&bar.v_full[vs], TILE_BYTES);
+          for (int c = 0; c < C::NH; ++c)
+            tma_load_4d(base + OFF_V + vs * TILE_BYTES + c * HALF_BYTES, &tm_v, &bar.v_full[vs],
+                        c * 64, w.hk, kt * BN, w.b);
+        }
       }
       if (bar.abort) {
-        for (int n = max(0, n_tiles - VST); n < n_tiles; ++n)
+        if (nq > 0) mbar_wait_final(&bar.q_full, (nq - 1) & 1, a.timeout_ns);
+        for (int n = max(0, g - VST); n < g; ++n)
           mbar_wait_final(&bar.v_full[n % VST], (n / VST) & 1, a.timeout_ns);
       }
     }
   } else if (warp == WARP_MMA) {
     // ------------------------------------------------ MMA issuer
-    // Rows that use_half_path turns down (every dense mask) run the plain loop; the
-    // flag-aware loop is a separate instantiation, so the plain one carries no per-tile
-    // flag handling (the issue loop is sensitive to any extra work).
-    const bool halves = use_half_path(pl.kt_cls + beg, n_tiles, HALF_SHARE, lane);
-    if (lane == 0) {
-      constexpr uint32_t IDESC_QK = idesc_bf16(BM, BN, 0, 0);
-      constexpr uint32_t IDESC_QK_HALF = idesc_bf16(BM, BN / 2, 0, 0);
-      constexpr uint32_t IDESC_PV = idesc_bf16(BM, HD, 0, 1);
-      const uint64_t dq0 = kmajor_desc(base_u32 + OFF_Q, 0);
-      const uint64_t dk0 = kmajor_desc(base_u32 + OFF_K, 0);
-      const uint64_t dv0 = mnmajor_desc(base_u32 + OFF_V, 0);
-      // P_j sits (bf16 pairs) in the first 64 TMEM columns of S buffer j % 3.  S_{j+3}
-      // reuses that buffer; it is issued after PV_j and tcgen05 MMAs of one thread run
-      // in issue order, so PV_j has read P_j before S_{j+3} overwrites it (and PV_j
-      // waited for the softmax of tile j, so S_j was consumed).
-      auto issue_pv = [&](int j, int empty) {
-        const int sb = j % NSB;
-        const int vs = j % VST;
-        mbar_wait(&bar.p_ready[sb], (j / NSB) & 1, wc);
-        mbar_wait(&bar.v_full[vs], (j / VST) & 1, wc);
-        tc_fence_after();
-        const uint64_t dv = dv0 + vs * stage_step(TILE_BYTES);
-        const uint32_t ta = tmem + TM_S0 + sb * BN;
-        if (empty == 0) {
+    // The per-tile issue loops are those of a one-unit CTA (the issue loop is sensitive to
+    // any per-tile extra work); unit transitions sit outside them.  A unit's first two S
+    // MMAs go out as soon as its Q has landed; its first PV (which overwrites O) waits
+    // until the softmax warps have read the previous unit's O (o_free), so those S MMAs
+    // overlap the previous unit's epilogue.  The whole warp walks the units
+    // (use_half_path is warp-wide); lane 0 issues.
+    constexpr uint32_t IDESC_QK = idesc_bf16(BM, BN, 0, 0);
+    constexpr uint32_t IDESC_QK_HALF = idesc_bf16(BM, BN / 2, 0, 0);
+    constexpr uint32_t IDESC_PV = idesc_bf16(BM, HD, 0, 1);
+    const uint64_t dq0 = kmajor_desc(base_u32 + OFF_Q, 0);
+    const uint64_t dk0 = kmajor_desc(base_u32 + OFF_K, 0);
+    const uint64_t dv0 = mnmajor_desc(base_u32 + OFF_V, 0);
+    // P_j sits (bf16 pairs) in the first 64 TMEM columns of S buffer j % 3.  S_{j+3}
+    // reuses that buffer; it is issued after PV_j and tcgen05 MMAs of one thread run
+    // in issue order, so PV_j has read P_j before S_{j+3} overwrites it.
+    auto issue_pv = [&](int j, int j0, int empty) {
+      const int sb = j % NSB;
+      const int vs = j % VST;
+      mbar_wait(&bar.p_ready[sb], (j / NSB) & 1, wc);
+      mbar_wait(&bar.v_full[vs], (j / VST) & 1, wc);
+      tc_fence_after();
+      const uint64_t dv = dv0 + vs * stage_step(TILE_BYTES);
+      const uint32_t ta = tmem + TM_S0 + sb * BN;
+      if (empty == 0) {
 #pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk)
-            umma_bf16_ts(tmem + TM_O, ta + kk * 8, dv + mnmajor_step(kk), IDESC_PV,
-                         (j > 0 || kk > 0) ? 1u : 0u);
-        } else {
-          // the four k-steps of the other key half only
-          const int k0 = empty == 1 ? 4 : 0;
-#pragma unroll
-          for (int kk = 0; kk < BN / 32; ++kk)
-            umma_bf16_ts(tmem + TM_O, ta + (k0 + kk) * 8, dv + mnmajor_step(k0 + kk), IDESC_PV,
-                         (j > 0 || kk > 0) ? 1u : 0u);
-        }
-        umma_commit(&bar.pv_done[sb]);
-        umma_commit(&bar.v_empty[vs]);
-      };
-      auto issue_s = [&](int n, int empty) {
-        const int sb = n % NSB;
-        const int ks = n % KST;
-        mbar_wait(&bar.k_full[ks], (n / KST) & 1, wc);
-        tc_fence_after();
-        const uint64_t dk = dk0 + ks * stage_step(TILE_BYTES);
-        const uint32_t td = tmem + TM_S0 + sb * BN;
-        if (empty == 0) {
-#pragma unroll
-          for (int kk = 0; kk < HD / 16; ++kk)
-            umma_bf16_ss(td, dq0 + kmajor_step(kk, HALF_BYTES), dk + kmajor_step(kk, HALF_BYTES),
-                         IDESC_QK, kk > 0 ? 1u : 0u);
-        } else {
-          // one key half only: its 64 K rows into its 64 S columns
-          const int hf = empty == 1 ? 1 : 0;
-#pragma unroll
-          for (int kk = 0; kk < HD / 16; ++kk)
-            umma_bf16_ss(td + hf * 64, dq0 + kmajor_step(kk, HALF_BYTES),
-                         dk + hf * ROWS64_STEP + kmajor_step(kk, HALF_BYTES), IDESC_QK_HALF,
-                         kk > 0 ? 1u : 0u);
-        }
-        umma_commit(&bar.s_full[sb]);
-        umma_commit(&bar.k_empty[ks]);
-      };
-      mbar_wait(&bar.q_full, 0, wc);
-      if (!halves) {
-        for (int n = 0; n < n_tiles; ++n) {
-          issue_s(n, 0);
-          if (n >= 2) issue_pv(n - 2, 0);
-        }
-        for (int j = max(0, n_tiles - 2); j < n_tiles; ++j) issue_pv(j, 0);
+        for (int kk = 0; kk < BN / 16; ++kk)
+          umma_bf16_ts(tmem + TM_O, ta + kk * 8, dv + mnmajor_step(kk), IDESC_PV,
+                       (j > j0 || kk > 0) ? 1u : 0u);
       } else {
-        // The flags reach the issuer one tile ahead of use (a load consumed right away
-        // holds the issue of the next MMAs back) and stay in a register history, two
-        // bits per tile, for the PV MMA two tiles later.
-        int e_next = n_tiles > 0 ? __ldg(pl.kt_cls + beg) : 0;
-        uint32_t hist = 0u;
-        for (int n = 0; n < n_tiles; ++n) {
-          const int empty = entry_empty_halves(e_next);
-          hist = (hist << 2) | static_cast<uint32_t>(empty);
-          if (n + 1 < n_tiles) e_next = __ldg(pl.kt_cls + beg + n + 1);
-          issue_s(n, empty);
-          if (n >= 2) issue_pv(n - 2, (hist >> 4) & 3);
-        }
-        for (int j = max(0, n_tiles - 2); j < n_tiles; ++j)
-          issue_pv(j, (hist >> (2 * (n_tiles - 1 - j))) & 3);
+        const int k0 = empty == 1 ? 4 : 0;
+#pragma unroll
+        for (int kk = 0; kk < BN / 32; ++kk)
+          umma_bf16_ts(tmem + TM_O, ta + (k0 + kk) * 8, dv + mnmajor_step(k0 + kk), IDESC_PV,
+                       (j > j0 || kk > 0) ? 1u : 0u);
       }
+      umma_commit(&bar.pv_done[sb]);
+      umma_commit(&bar.v_empty[vs]);
+    };
+    auto issue_s = [&](int n, int empty) {
+      const int sb = n % NSB;
+      const int ks = n % KST;
+      mbar_wait(&bar.k_full[ks], (n / KST) & 1, wc);
+      tc_fence_after();
+      const uint64_t dk = dk0 + ks * stage_step(TILE_BYTES);
+      const uint32_t td = tmem + TM_S0 + sb * BN;
+      if (empty == 0) {
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk)
+          umma_bf16_ss(td, dq0 + kmajor_step(kk, HALF_BYTES), dk + kmajor_step(kk, HALF_BYTES),
+                       IDESC_QK, kk > 0 ? 1u : 0u);
+      } else {
+        const int hf = empty == 1 ? 1 : 0;
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk)
+          umma_bf16_ss(td + hf * 64, dq0 + kmajor_step(kk, HALF_BYTES),
+                       dk + hf * ROWS64_STEP + kmajor_step(kk, HALF_BYTES), IDESC_QK_HALF,
+                       kk > 0 ? 1u : 0u);
+      }
+      umma_commit(&bar.s_full[sb]);
+      umma_commit(&bar.k_empty[ks]);
+    };
+    int g = 0, nq = 0;
+    for (int k = 0;; ++k) {
+      const int u = take_unit(k, true);
+      if (u >= n_units) break;
+      const Unit w = decode(u);
+      if (w.n == 0) continue;
+      const bool halves = use_half_path(pl.kt_cls + w.beg, w.n, HALF_SHARE, lane);
+      if (lane == 0 && !bar.abort) {
+        mbar_wait(&bar.q_full, nq & 1, wc);
+        const int g0 = g, g1 = g + w.n;
+        const int gs = min(g0 + 2, g1);   // the S MMAs issued before the o_free wait
+        if (!halves) {
+          for (int n = g0; n < gs; ++n) issue_s(n, 0);
+          if (nq > 0) mbar_wait(&bar.o_free, (nq - 1) & 1, wc);
+          for (int n = gs; n < g1; ++n) {
+            issue_s(n, 0);
+            issue_pv(n - 2, g0, 0);
+          }
+          umma_commit(&bar.q_empty);   // the unit's last S has read Q
+          for (int j = max(g0, g1 - 2); j < g1; ++j) issue_pv(j, g0, 0);
+        } else {
+          // flags one tile ahead of use, then a register history for the PV two tiles later
+          int e_next = __ldg(pl.kt_cls + w.beg);
+          uint32_t hist = 0u;
+          for (int n = g0; n < g1; ++n) {
+            const int empty = entry_empty_halves(e_next);
+            hist = (hist << 2) | static_cast<uint32_t>(empty);
+            if (n + 1 < g1) e_next = __ldg(pl.kt_cls + w.beg + (n + 1 - g0));
+            issue_s(n, empty);
+            if (n == gs - 1 && nq > 0) mbar_wait(&bar.o_free, (nq - 1) & 1, wc);
+            if (n >= g0 + 2) issue_pv(n - 2, g0, (hist >> 4) & 3);
+          }
+          umma_commit(&bar.q_empty);
+          for (int j = max(g0, g1 - 2); j < g1; ++j)
+            issue_pv(j, g0, (hist >> (2 * (g1 - 1 - j))) & 3);
+        }
+      }
+      // the other lanes wait here, suspended, instead of spinning on the next unit's slot
+      // while lane 0 issues (divergent lanes of a warp share its issue slots)
+      __syncwarp();
+      g += w.n;
+      ++nq;
     }
   } else {
     // ------------------------------------------------ softmax warps 0-7
     const int quarter = warp & 3;          // TMEM lane quarter
     const int half = warp >> 2;            // key columns [64 * half, 64 * half + 64)
     const int t = quarter * 32 + lane;     // row within the tile = TMEM lane
-    const int i = qt * BM + t;
     const uint32_t quarter_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const uint32_t lane_addr = quarter_addr + half * 64;
-    const RowSpan sp = row_span(a.mask, min(i, S - 1));
-    MapCursor mcur;
     const float sl2 = dm.scale_log2;
     float* red = reinterpret_cast<float*>(base + OFF_RED);  // [parity][half][row]
-    float m_run = -INFINITY;
-    float l_run = 0.f;
-
-    // One key tile; IDLE: this warp's key half holds no pair of the tile (no S to read,
-    // no P to write, only the row-max exchange and the O rescale).  Two instantiations
-    // keep the common path's code exactly that of a full-width tile.
-    auto tile_step = [&](int n, auto idle_c) {
-      constexpr bool IDLE = decltype(idle_c)::value;
-      const int st = n % NSB;             // S buffer
-      const uint32_t ph = (n / NSB) & 1;
-      const int rp = n & 1;               // max-exchange parity
-      float s[64];
-      float mx = -INFINITY;
-      if constexpr (!IDLE) {
-        const int kt = __ldg(pl.kt_idx + beg + n);
-        const int e = __ldg(pl.kt_cls + beg + n);
-        const int c0 = kt * BN + half * 64;
-        const bool masked = entry_class(e) != LCA_TILE_FULL || kt * BN + BN > S;
-        uint32_t bits[2] = {0u, 0u};
-        if (masked && i < S) row_tile_bits<2>(a.mask, hm, i, c0, sp, bits, &mcur);
-        mbar_wait(&bar.s_full[st], ph, wc);
-        __syncwarp();
-        tc_fence_after();
-        uint32_t r[64];
-        tmem_ld64(lane_addr + TM_S0 + st * BN, r);
+    int g = 0;    // tile counter (S buffers, barrier phases)
+    int x = 0;    // row-max / row-sum exchange counter (red parity)
+    for (int k = 0;; ++k) {
+      const int u = take_unit(k, true);
+      if (u >= n_units) break;
+      const Unit w = decode(u);
+      const int i = w.qt * BM + t;
+      if (w.n == 0) {   // no allowed key anywhere in the tile: O = 0, LSE = -inf
+        if (i < S) {
+          uint4* dst = reinterpret_cast<uint4*>(a.o + (static_cast<int64_t>(w.b) * S + i) *
+                                                          a.o_row_stride +
+                                                static_cast<int64_t>(w.h) * HD + half * OCOLS);
 #pragma unroll
-        for (int x = 0; x < 64; ++x) s[x] = __uint_as_float(r[x]);
-        if (masked) {
-#pragma unroll
-          for (int x = 0; x < 64; ++x)
-            if (!((bits[x >> 5] >> (x & 31)) & 1u)) s[x] = -INFINITY;
+          for (int v = 0; v < OCOLS / 8; ++v) dst[v] = make_uint4(0u, 0u, 0u, 0u);
+          if (half == 0) a.lse[(static_cast<int64_t>(w.b) * dm.h_q + w.h) * S + i] = -INFINITY;
         }
-        float mq[8];
+        continue;
+      }
+      const RowSpan sp = row_span(a.mask, min(i, S - 1));
+      MapCursor mcur;
+      float m_run = -INFINITY;
+      float l_run = 0.f;
+      auto tile_step = [&](int n, auto idle_c) {
+        constexpr bool IDLE = decltype(idle_c)::value;
+        const int gn = g + n;
+        const int st = gn % NSB;             // S buffer
+        const uint32_t ph = (gn / NSB) & 1;
+        const int rp = (x + n) & 1;          // exchange parity
+        float s[64];
+        float mx = -INFINITY;
+        if constexpr (!IDLE) {
+          const int kt = __ldg(pl.kt_idx + w.beg + n);
+          const int e = __ldg(pl.kt_cls + w.beg + n);
+          const int c0 = kt * BN + half * 64;
+          const bool masked = entry_class(e) != LCA_TILE_FULL || kt * BN + BN > S;
+          uint32_t bits[2] = {0u, 0u};
+          if (masked && i < S) row_tile_bits<2>(a.mask, w.hm, i, c0, sp, bits, &mcur);
+          mbar_wait(&bar.s_full[st], ph, wc);
+          __syncwarp();
+          tc_fence_after();
+          uint32_t r[64];
+          tmem_ld64(lane_addr + TM_S0 + st * BN, r);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) mq[k] = s[k];
+          for (int xx = 0; xx < 64; ++xx) s[xx] = __uint_as_float(r[xx]);
+          if (masked) {
 #pragma unroll
-        for (int x = 8; x < 64; x += 8)
+            for (int xx = 0; xx < 64; ++xx)
+              if (!((bits[xx >> 5] >> (xx & 31)) & 1u)) s[xx] = -INFINITY;
+          }
+          float mq[8];
 #pragma unroll
-          for (int k = 0; k < 8; ++k) mq[k] = fmaxf(mq[k], s[x + k]);
-        mx = fmaxf(fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])),
-                   fmaxf(fmaxf(mq[4], mq[5]), fmaxf(mq[6], mq[7])));
+          for (int kk = 0; kk < 8; ++kk) mq[kk] = s[kk];
+#pragma unroll
+          for (int xx = 8; xx < 64; xx += 8)
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) mq[kk] = fmaxf(mq[kk], s[xx + kk]);
+          mx = fmaxf(fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])),
+                     fmaxf(fmaxf(mq[4], mq[5]), fmaxf(mq[6], mq[7])));
+        } else {
+          mbar_wait(&bar.s_full[st], ph, wc);
+        }
+        red[(rp * 2 + half) * BM + t] = mx;
+        named_bar_sync(BAR_SOFTMAX, SOFTMAX_THREADS);
+        mx = fmaxf(mx, red[(rp * 2 + (half ^ 1)) * BM + t]);
+        const float mt = mx * sl2;
+        float alpha = 1.f;
+        bool rescale = false;
+        if (mt > m_run + RESCALE_THRESHOLD) {
+          rescale = (m_run != -INFINITY);
+          alpha = ex2_approx(m_run - mt);
+          l_run *= alpha;
+          m_run = mt;
+        }
+        if (__any_sync(0xFFFFFFFFu, rescale)) {
+          // O holds this unit's P V so far: wait for its last PV, scale, store back
+          const int pj = gn - 1;
+          mbar_wait(&bar.pv_done[pj % NSB], (pj / NSB) & 1, wc);
+          __syncwarp();
+          tc_fence_after();
+          const float f = rescale ? alpha : 1.f;
+          uint32_t o[OCOLS];
+          tmem_ldn<OCOLS>(quarter_addr + TM_O + half * OCOLS, o);
+#pragma unroll
+          for (int xx = 0; xx < OCOLS; ++xx) o[xx] = __float_as_uint(__uint_as_float(o[xx]) * f);
+          tmem_stn<OCOLS>(quarter_addr + TM_O + half * OCOLS, o);
+        }
+        if constexpr (!IDLE) {
+          const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+          float ls[8];
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) ls[kk] = 0.f;
+#pragma unroll
+          for (int xx = 0; xx < 64; ++xx) {
+            s[xx] = ex2_approx(fmaf(s[xx], sl2, -m_use));
+            ls[xx & 7] += s[xx];
+          }
+          l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+          uint32_t pk[32];
+#pragma unroll
+          for (int xx = 0; xx < 32; ++xx) pk[xx] = pack_bf16x2(s[2 * xx], s[2 * xx + 1]);
+          tmem_st32(quarter_addr + TM_S0 + st * BN + half * 32, pk);
+        }
+        tc_fence_before();
+        mbar_arrive(&bar.p_ready[st]);
+      };
+      if (!use_half_path(pl.kt_cls + w.beg, w.n, HALF_SHARE, lane)) {
+        for (int n = 0; n < w.n; ++n) tile_step(n, std::false_type{});
       } else {
-        mbar_wait(&bar.s_full[st], ph, wc);
+        for (int n = 0; n < w.n; ++n) {
+          if ((entry_empty_halves(__ldg(pl.kt_cls + w.beg + n)) >> half) & 1)
+            tile_step(n, std::true_type{});
+          else
+            tile_step(n, std::false_type{});
+        }
       }
-      red[(rp * 2 + half) * BM + t] = mx;
-      named_bar_sync(BAR_SOFTMAX, SOFTMAX_THREADS);
-      mx = fmaxf(mx, red[(rp * 2 + (half ^ 1)) * BM + t]);
-      const float mt = mx * sl2;
-      float alpha = 1.f;
-      bool rescale = false;
-      if (mt > m_run + RESCALE_THRESHOLD) {
-        rescale = (m_run != -INFINITY);
-        alpha = ex2_approx(m_run - mt);
-        l_run *= alpha;
-        m_run = mt;
-      }
-      if (__any_sync(0xFFFFFFFFu, rescale)) {
-        // O holds P_0..P_{n-1} V: wait for the last PV, scale this half row, store back
-        const int pj = n - 1;
+
+      // ---- epilogue: O = acc / l (bf16), LSE = (m + log2 l) * ln 2; then O is free
+      {
+        const int pj = g + w.n - 1;
         mbar_wait(&bar.pv_done[pj % NSB], (pj / NSB) & 1, wc);
         __syncwarp();
         tc_fence_after();
-        const float f = rescale ? alpha : 1.f;
-        uint32_t o[OCOLS];
-        tmem_ldn<OCOLS>(quarter_addr + TM_O + half * OCOLS, o);
-#pragma unroll
-        for (int x = 0; x < OCOLS; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * f);
-        tmem_stn<OCOLS>(quarter_addr + TM_O + half * OCOLS, o);
       }
-      if constexpr (!IDLE) {
-        const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-        float ls[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) ls[k] = 0.f;
-#pragma unroll
-        for (int x = 0; x < 64; ++x) {
-          s[x] = ex2_approx(fmaf(s[x], sl2, -m_use));
-          ls[x & 7] += s[x];
-        }
-        l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
-        // P (bf16 pairs) into the first 64 columns of this S buffer; both halves of the
-        // row finished reading S before the max exchange barrier above
-        uint32_t pk[32];
-#pragma unroll
-        for (int x = 0; x < 32; ++x) pk[x] = pack_bf16x2(s[2 * x], s[2 * x + 1]);
-        tmem_st32(quarter_addr + TM_S0 + st * BN + half * 32, pk);
-      }
-      tc_fence_before();
-      mbar_arrive(&bar.p_ready[st]);
-    };
-    if (!use_half_path(pl.kt_cls + beg, n_tiles, HALF_SHARE, lane)) {
-      for (int n = 0; n < n_tiles; ++n) tile_step(n, std::false_type{});
-    } else {
-      for (int n = 0; n < n_tiles; ++n) {
-        if ((entry_empty_halves(__ldg(pl.kt_cls + beg + n)) >> half) & 1)
-          tile_step(n, std::true_type{});
-        else
-          tile_step(n, std::false_type{});
-      }
-    }
-
-    // ---- epilogue: O = acc / l (bf16), LSE = (m + log2 l) * ln 2
-    if (n_tiles > 0) {
-      const int pj = n_tiles - 1;
-      mbar_wait(&bar.pv_done[pj % NSB], (pj / NSB) & 1, wc);
-      __syncwarp();
-      tc_fence_after();
-    }
-    // row-sum exchange in the slots of parity n_tiles & 1: last written for tile
-    // n_tiles - 2, whose reads both threads finished before the last tile's barrier
-    const int pe = n_tiles & 1;
-    red[(pe * 2 + half) * BM + t] = l_run;
-    named_bar_sync(BAR_SOFTMAX, SOFTMAX_THREADS);
-    const float l_tot = l_run + red[(pe * 2 + (half ^ 1)) * BM + t];
-    const float inv = (l_tot > 0.f) ? 1.f / l_tot : 0.f;
-    uint32_t o[OCOLS];
-    if (n_tiles > 0) {
+      const int pe = (x + w.n) & 1;
+      red[(pe * 2 + half) * BM + t] = l_run;
+      named_bar_sync(BAR_SOFTMAX, SOFTMAX_THREADS);
+      const float l_tot = l_run + red[(pe * 2 + (half ^ 1)) * BM + t];
+      const float inv = (l_tot > 0.f) ? 1.f / l_tot : 0.f;
+      uint32_t o[OCOLS];
       tmem_ldn<OCOLS>(quarter_addr + TM_O + half * OCOLS, o);
-    } else {
+      tc_fence_before();
+      mbar_arrive(&bar.o_free);
+      if (i < S) {
+        __nv_bfloat16* orow = a.o + (static_cast<int64_t>(w.b) * S + i) * a.o_row_stride +
+                              static_cast<int64_t>(w.h) * HD + half * OCOLS;
+        uint4* dst = reinterpret_cast<uint4*>(orow);
 #pragma unroll
-      for (int x = 0; x < OCOLS; ++x) o[x] = 0u;
-    }
-    if (i < S) {
-      __nv_bfloat16* orow = a.o + (static_cast<int64_t>(b) * S + i) * a.o_row_stride +
-                            static_cast<int64_t>(h) * HD + half * OCOLS;
-      uint4* dst = reinterpret_cast<uint4*>(orow);
-#pragma unroll
-      for (int v = 0; v < OCOLS / 8; ++v) {
-        const int x = v * 8;
-        uint4 w;
-        w.x = pack_bf16x2(__uint_as_float(o[x + 0]) * inv, __uint_as_float(o[x + 1]) * inv);
-        w.y = pack_bf16x2(__uint_as_float(o[x + 2]) * inv, __uint_as_float(o[x + 3]) * inv);
-        w.z = pack_bf16x2(__uint_as_float(o[x + 4]) * inv, __uint_as_float(o[x + 5]) * inv);
-        w.w = pack_bf16x2(__uint_as_float(o[x + 6]) * inv, __uint_as_float(o[x + 7]) * inv);
-        dst[v] = w;
+        for (int v = 0; v < OCOLS / 8; ++v) {
+          const int xx = v * 8;
+          uint4 ww;
+          ww.x = pack_bf16x2(__uint_as_float(o[xx + 0]) * inv, __uint_as_float(o[xx + 1]) * inv);
+          ww.y = pack_bf16x2(__uint_as_float(o[xx + 2]) * inv, __uint_as_float(o[xx + 3]) * inv);
+          ww.z = pack_bf16x2(__uint_as_float(o[xx + 4]) * inv, __uint_as_float(o[xx + 5]) * inv);
+          ww.w = pack_bf16x2(__uint_as_float(o[xx + 6]) * inv, __uint_as_float(o[xx + 7]) * inv);
+          dst[v] = ww;
+        }
+        if (half == 0) {
+          const float lse = (l_tot > 0.f) ? (m_run + __log2f(l_tot)) * 0.69314718055994531f
+                                          : -INFINITY;
+          a.lse[(static_cast<int64_t>(w.b) * dm.h_q + w.h) * S + i] = lse;
+        }
       }
-      if (half == 0) {
-        const float lse = (l_tot > 0.f) ? (m_run + __log2f(l_tot)) * 0.69314718055994531f
-                                        : -INFINITY;
-        a.lse[(static_cast<int64_t>(b) * dm.h_q + h) * S + i] = lse;
-      }
+      g += w.n;
+      x += w.n + 1;
     }
   }
 
@@ -478,21 +581,24 @@ size_t fwd_smem_bytes() { return Cfg<128>::SMEM_BYTES; }
 
 template <int HD>
 static cudaError_t launch_fwd_hd(const CUtensorMap& tq, const CUtensorMap& tk,
-                                 const CUtensorMap& tv, const FwdArgs& args, int n_blocks,
+                                 const CUtensorMap& tv, const FwdArgs& args, int n_ctas,
                                  cudaStream_t st) {
   constexpr uint32_t smem = Cfg<HD>::SMEM_BYTES;
   cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<HD>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  attn_fwd_kernel<HD><<<n_blocks, NUM_THREADS, smem, st>>>(tq, tk, tv, args);
+  attn_fwd_kernel<HD><<<n_ctas, NUM_THREADS, smem, st>>>(tq, tk, tv, args);
   return cudaGetLastError();
 }
 
 cudaError_t launch_attn_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const FwdArgs& args, int n_blocks, cudaStream_t st) {
-  if (n_blocks == 0) return cudaSuccess;
-  if (args.dims.head_dim == 64) return launch_fwd_hd<64>(tq, tk, tv, args, n_blocks, st);
-  return launch_fwd_hd<128>(tq, tk, tv, args, n_blocks, st);
+                            const FwdArgs& args, int n_ctas, cudaStream_t st) {
+  if (args.n_units == 0) return cudaSuccess;
+  // the unit counter starts at 0 for every launch
+  cudaError_t e = cudaMemsetAsync(args.unit_counter, 0, sizeof(unsigned int), st);
+  if (e != cudaSuccess) return e;
+  if (args.dims.head_dim == 64) return launch_fwd_hd<64>(tq, tk, tv, args, n_ctas, st);
+  return launch_fwd_hd<128>(tq, tk, tv, args, n_ctas, st);
 }
 
 }  // namespace lca

@@ -18,6 +18,8 @@ struct FwdArgs {
   int64_t o_row_stride;
   unsigned int* err;
   uint64_t timeout_ns;
+  int n_units;                  // (query tile, query head, batch entry) units
+  unsigned int* unit_counter;   // next unit to hand out (zeroed before the launch)
 };
 
 struct BwdArgs {
@@ -44,8 +46,10 @@ struct BwdArgs {
 };
 
 size_t fwd_smem_bytes();
+// n_ctas persistent CTAs (at most one per SM) take the args.n_units units from
+// args.unit_counter, which the launch zeroes first on `st`.
 cudaError_t launch_attn_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const FwdArgs& args, int n_blocks, cudaStream_t st);
+                            const FwdArgs& args, int n_ctas, cudaStream_t st);
 
 cudaError_t launch_bwd_preprocess(const BwdArgs& args, cudaStream_t st);
 // dK/dV (n_kv CTAs: one per KV head and key tile) and dQ (n_q CTAs: one per query head

@@ -151,3 +151,27 @@ def test_head_dim_64(hq, hkv, b):
         o_ref, lse_ref = oracle.attn_fwd_ref(*host[:3], desc)
         check_o(o, o_ref, f"d64 {desc.name}")
         check_lse(lse, lse_ref, f"d64 {desc.name}")
+
+
+def test_concurrent_forwards_share_a_plan():
+    """The persistent forward takes its units from a counter of the plan; calls on two
+    streams that share one plan each get their own counter and give the results of the
+    calls run one after the other (bit-identical: a unit is computed by one CTA)."""
+    s, hq, hkv = 4096, 16, 2
+    host, dev = make_inputs(1, s, hq, hkv, seed=88)
+    q, k, v, _ = dev
+    plan = lca.mask_build(I.make_desc(I.CAUSAL_DOCUMENT, s, doc_seed=8))
+    ref = [lca.attn_fwd(plan, q, k, v) for _ in range(2)]
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream() for _ in range(2)]
+    outs = []
+    for st in streams:
+        with torch.cuda.stream(st):
+            outs.append(lca.attn_fwd(plan, q, k, v, stream=st))
+    torch.cuda.synchronize()
+    assert lca.last_device_error() == 0
+    for (o, l), (o_ref, l_ref) in zip(outs, ref):
+        assert torch.equal(o, o_ref) and torch.equal(l, l_ref)
+    o_ref_host, lse_ref_host = oracle.attn_fwd_ref(*host[:3], plan.desc)
+    check_o(to_np(outs[1][0]), o_ref_host, "concurrent")
+    check_lse(to_np(outs[1][1]), lse_ref_host, "concurrent")
