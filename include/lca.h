@@ -259,10 +259,11 @@ lca_status lca_attn_bwd(const lca_plan* plan, const lca_shape* shape, const void
                         size_t ws_bytes, float softmax_scale, int flags, void* stream);
 
 /* Backward pass that allocates nothing, for callers that cannot allocate device memory
- * when they run the backward (inside CUDA-graph capture, under allocators that forbid
- * side allocations, or in runtimes that only hand out the op's own tensors).  The
- * attention method itself has no counterpart of this call: it only changes where the
- * workspace of lca_attn_bwd comes from.
+ * when they run the backward: code under a caching or pooled allocator that forbids
+ * allocations outside its own pool, runtimes that hand an op only its own input and
+ * output tensors, and programs that reserve all device memory up front.  The attention
+ * method itself has no counterpart of this call: it only changes where the workspace
+ * of lca_attn_bwd comes from.
  *
  * Same arguments, preconditions and results as lca_attn_bwd (flags 0), except that
  * the workspace is a fixed 64 MiB buffer compiled into the library (a file-scope
@@ -274,7 +275,7 @@ lca_status lca_attn_bwd(const lca_plan* plan, const lca_shape* shape, const void
  * that grows on first use).
  * The first call on a device looks the buffer's device address up (with that device
  * current; again after the device's context was torn down and re-created, e.g. by
- * cudaDeviceReset); make that first call before any stream capture.
+ * cudaDeviceReset).
  * Every call on a device shares the one buffer: each call overwrites every entry it
  * reads, so nothing needs clearing, but calls whose work overlaps on the GPU (other
  * streams, other threads) race on it and must be serialised by the caller. */

@@ -3,9 +3,9 @@
 //
 // lca_attn_bwd needs a caller-provided workspace (per-row LSE*log2(e) and
 // D = rowsum(dO * O), fp32, rows padded to whole 128-row tiles).  Some callers cannot
-// call cudaMalloc at that point: code running while a CUDA graph is being captured on
-// their stream, custom allocators that forbid side allocations, or runtimes that hand
-// out only the tensors of the op itself.  This entry point takes the workspace from a
+// call cudaMalloc at that point: code under a caching or pooled allocator that forbids
+// allocations outside its pool, runtimes that hand out only the tensors of the op
+// itself, or programs that reserve all device memory when they start.  This entry point takes the workspace from a
 // fixed buffer compiled into the library instead, and otherwise runs exactly the
 // lca_attn_bwd path.
 #include <cuda.h>

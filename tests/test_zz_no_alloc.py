@@ -1,6 +1,6 @@
 """lca_attn_bwd_noalloc, the backward for callers that cannot allocate device memory
-while it runs (CUDA-graph capture, allocators that forbid side allocations, runtimes
-that only hand out the op's own tensors).  Through the C ABI it must give the results
+while it runs (pooled allocators that forbid side allocations, runtimes that only hand
+out the op's own tensors, programs that reserve all device memory up front).  Through the C ABI it must give the results
 of lca_attn_bwd and of the fp64 oracle, on consecutive calls that share its built-in
 workspace.
 
