@@ -7,10 +7,11 @@
 // Persistent CTAs, at most one per SM, work through units (one 128-row query tile of
 // one query head and batch entry, with the tile's list of non-skipped key tiles from
 // the tile plan).  Units are handed out in longest-first order by a global counter: the
-// K producer thread takes the next unit when it starts loading that unit's K tiles and
-// passes it to the other roles through a ring of shared-memory slots, so an SM moves on
-// to its next unit without a CTA exit, launch and prologue, and the next unit's loads
-// and first S MMAs overlap the end of the current one.  Roles:
+// K producer warp takes the next unit when it starts loading that unit's K tiles,
+// decodes it and passes it to the other roles through a ring of shared-memory slots, so
+// an SM moves on to its next unit without a CTA exit, launch and prologue, and the next
+// unit's loads, first S MMAs and first softmax tile overlap the end of the current one.
+// Roles:
 //   warp 8      unit fetcher and K producer: the K tiles of every unit into a 3-stage
 //               ring (the ring and every barrier phase follow one tile counter across
 //               units), the next unit's Q prefetched into L2;
@@ -28,7 +29,8 @@
 //               maxima through shared memory, online softmax in fp32 with exp2, write P
 //               (bf16 pairs) back into the TMEM columns of S_n for the PV MMA, rescale
 //               the O accumulator in TMEM when the running max moves by more than 2^8
-//               (exact after the final 1/l normalisation), then the unit's epilogue.
+//               (exact after the final 1/l normalisation); the next unit's first tile,
+//               then this unit's epilogue.
 // In a row of at least 64 plan entries of which at least a quarter flag one key half of
 // their tile as empty (no allowed pair: block maps on a grid finer than the tile, ragged tails),
 // such a tile runs at half width: S is an N = 64 MMA on the other half's keys, PV takes
@@ -76,7 +78,7 @@ struct Cfg {
   static constexpr uint32_t OFF_K = OFF_Q + TILE_BYTES;       // KST stages
   static constexpr uint32_t OFF_V = OFF_K + KST * TILE_BYTES; // VST stages
   static constexpr uint32_t OFF_BAR = OFF_V + VST * TILE_BYTES;
-  static constexpr uint32_t OFF_RED = OFF_BAR + 320;          // row-max / row-sum exchange
+  static constexpr uint32_t OFF_RED = OFF_BAR + 400;          // row-max / row-sum exchange
   static constexpr uint32_t SMEM_BYTES = OFF_RED + 2 * 2 * BM * 4;
   static constexpr int OCOLS = HD / 2;                        // O columns per softmax thread
   static_assert(HD == 64 || HD == 128, "head_dim 64 or 128");
@@ -100,6 +102,11 @@ __device__ __forceinline__ void tmem_stn(uint32_t taddr, const uint32_t (&r)[N])
 constexpr int UR = 4;                 // unit ring slots
 constexpr int UNIT_READERS = 10;      // V producer, MMA warp, eight softmax warps
 
+// A unit as the fetcher decodes it: query head, KV head, map head, query tile, batch
+// entry, its row list [beg, beg + n) in the plan, and whether that list runs the
+// half-width path.  n < 0 marks the end of the work.
+struct Unit { int h, hk, hm, qt, b, beg, n, halves; };
+
 struct Bars {
   uint64_t q_full, q_empty, o_free;
   uint64_t unit_full[UR], unit_empty[UR];
@@ -108,9 +115,28 @@ struct Bars {
   uint64_t s_full[NSB], p_ready[NSB], pv_done[NSB];
   uint32_t tmem_base;
   int abort;
-  int unit[UR];
+  Unit unit[UR];
 };
-static_assert(sizeof(Bars) <= 320, "barrier block overflows its shared-memory slot");
+static_assert(sizeof(Bars) <= 400, "barrier block overflows its shared-memory slot");
+
+// use_half_path for the unit fetcher, which runs it while the K ring drains: lists too
+// short for the half-width path are not read at all, longer ones with eight loads in
+// flight per lane.
+__device__ __forceinline__ bool fetch_half_path(const uint8_t* e, int n, int lane) {
+  if (n < 64) return false;   // half_path() needs at least 64 entries
+  int f = 0;
+  for (int x0 = 0; x0 < n; x0 += 256) {
+    int v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int x = x0 + 32 * j + lane;
+      v[j] = x < n ? __ldg(e + x) : 0;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) f += (v[j] & kEntryHalfFlags) != 0;
+  }
+  return half_path(__reduce_add_sync(0xFFFFFFFFu, f), n, HALF_SHARE);
+}
 
 __device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, int kk) {
   return desc_kmajor(tile, kk, HALF_BYTES);
@@ -146,10 +172,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   const int n_units = a.n_units;
 
   // A unit is one (query tile, query head, batch entry).  Units are handed out in
-  // longest-first order by a global counter: one thread (the K producer) takes the next
-  // unit when it starts loading that unit's K tiles and passes it to the other roles
-  // through a ring of UR shared-memory slots.
-  struct Unit { int h, hk, hm, qt, b, beg, n; };
+  // longest-first order by a global counter: the K producer warp takes the next unit when
+  // it starts loading that unit's K tiles, decodes it (its list pointers and half-width
+  // decision come from global memory) and passes the decoded unit to the other roles
+  // through a ring of UR shared-memory slots, so no other role waits for those loads.
   auto decode = [&](int u) {
     const int per_item = dm.heads_per_map * dm.batch;
     int item, rem;
@@ -163,6 +189,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     w.hk = w.h / dm.group;
     w.beg = __ldg(pl.rowptr + row);
     w.n = __ldg(pl.rowptr + row + 1) - w.beg;
+    w.halves = 0;
     return w;
   };
 
@@ -202,38 +229,52 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
   // The k-th unit of this CTA sits in ring slot k % UR.  Readers other than the fetcher:
   // the V producer, the MMA warp and the eight softmax warps (lane 0 of each arrives once
-  // its warp has read the slot).  A unit index >= n_units ends every role's loop.
+  // its warp has read the slot).  A unit with n < 0 ends every role's loop.
   // WHOLE: called by all 32 lanes of a warp (lane 0 arrives after the warp has read the
   // slot); otherwise by one lane alone, which arrives itself.
   auto take_unit = [&](int k, bool whole) {
     const int slot = k % UR;
     mbar_wait(&bar.unit_full[slot], (k / UR) & 1, wc);
-    const int u = bar.abort ? n_units : bar.unit[slot];
+    Unit w = bar.unit[slot];
+    if (bar.abort) w.n = -1;
     if (whole) {
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar.unit_empty[slot]);
     } else {
       mbar_arrive(&bar.unit_empty[slot]);
     }
-    return u;
+    return w;
   };
 
   // The K/V rings, the S buffers and every barrier phase follow one tile counter g across
   // units; every role walks the same unit sequence, so the counters agree.
   if (warp == WARP_PRODUCER) {
     // ------------------------------------------------ unit fetcher and K producer
+    // The whole warp fetches and decodes a unit (the half-width scan is warp-wide); lane
+    // 0 publishes it and loads its K tiles while the other lanes wait at the __syncwarp.
     if (lane == 0) {
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_q);
-      int g = 0;
-      for (int k = 0;; ++k) {
-        const int slot = k % UR;
-        if (k >= UR) mbar_wait(&bar.unit_empty[slot], (k / UR - 1) & 1, wc);
-        const int u = bar.abort ? n_units : static_cast<int>(atomicAdd(a.unit_counter, 1u));
-        bar.unit[slot] = u;
+    }
+    int g = 0;
+    for (int k = 0;; ++k) {
+      const int slot = k % UR;
+      if (k >= UR) mbar_wait(&bar.unit_empty[slot], (k / UR - 1) & 1, wc);
+      int u = 0;
+      if (lane == 0) u = bar.abort ? n_units : static_cast<int>(atomicAdd(a.unit_counter, 1u));
+      u = __shfl_sync(0xFFFFFFFFu, u, 0);
+      Unit w{};
+      w.n = -1;
+      if (u < n_units) {
+        w = decode(u);
+        w.halves = fetch_half_path(pl.kt_cls + w.beg, w.n, lane);
+      }
+      if (lane == 0) {
+        bar.unit[slot] = w;
         mbar_arrive(&bar.unit_full[slot]);
-        if (u >= n_units) break;
-        const Unit w = decode(u);
+      }
+      if (u >= n_units) break;
+      if (lane == 0) {
         // the unit's Q is loaded only after the previous unit's last S; prefetching it into
         // L2 now (this thread runs a few tiles ahead) shortens that load
         if (w.n > 0)
@@ -252,10 +293,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         c * 64, w.hk, kt * BN, w.b);
         }
       }
-      if (bar.abort) {  // let copies in flight land before the CTA exits
-        for (int n = max(0, g - KST); n < g; ++n)
-          mbar_wait_final(&bar.k_full[n % KST], (n / KST) & 1, a.timeout_ns);
-      }
+      __syncwarp();
+    }
+    if (lane == 0 && bar.abort) {  // let copies in flight land before the CTA exits
+      for (int n = max(0, g - KST); n < g; ++n)
+        mbar_wait_final(&bar.k_full[n % KST], (n / KST) & 1, a.timeout_ns);
     }
   } else if (warp == WARP_PRODUCER_V) {
     // ------------------------------------------------ Q and V producer
@@ -265,9 +307,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       tma_prefetch_desc(&tm_v);
       int g = 0, nq = 0;
       for (int k = 0;; ++k) {
-        const int u = take_unit(k, false);
-        if (u >= n_units) break;
-        const Unit w = decode(u);
+        const Unit w = take_unit(k, false);
+        if (w.n < 0) break;
         if (w.n == 0) continue;
         if (nq > 0) mbar_wait(&bar.q_empty, (nq - 1) & 1, wc);
         mbar_arrive_expect_tx(&bar.q_full, TILE_BYTES);
@@ -360,11 +401,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     };
     int g = 0, nq = 0;
     for (int k = 0;; ++k) {
-      const int u = take_unit(k, true);
-      if (u >= n_units) break;
-      const Unit w = decode(u);
+      const Unit w = take_unit(k, true);
+      if (w.n < 0) break;
       if (w.n == 0) continue;
-      const bool halves = use_half_path(pl.kt_cls + w.beg, w.n, HALF_SHARE, lane);
+      const bool halves = w.halves != 0;
       if (lane == 0 && !bar.abort) {
         mbar_wait(&bar.q_full, nq & 1, wc);
         const int g0 = g, g1 = g + w.n;
@@ -410,141 +450,151 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const uint32_t lane_addr = quarter_addr + half * 64;
     const float sl2 = dm.scale_log2;
     float* red = reinterpret_cast<float*>(base + OFF_RED);  // [parity][half][row]
-    int g = 0;    // tile counter (S buffers, barrier phases)
-    int x = 0;    // row-max / row-sum exchange counter (red parity)
-    for (int k = 0;; ++k) {
-      const int u = take_unit(k, true);
-      if (u >= n_units) break;
-      const Unit w = decode(u);
-      const int i = w.qt * BM + t;
-      if (w.n == 0) {   // no allowed key anywhere in the tile: O = 0, LSE = -inf
-        if (i < S) {
-          uint4* dst = reinterpret_cast<uint4*>(a.o + (static_cast<int64_t>(w.b) * S + i) *
-                                                          a.o_row_stride +
-                                                static_cast<int64_t>(w.h) * HD + half * OCOLS);
-#pragma unroll
-          for (int v = 0; v < OCOLS / 8; ++v) dst[v] = make_uint4(0u, 0u, 0u, 0u);
-          if (half == 0) a.lse[(static_cast<int64_t>(w.b) * dm.h_q + w.h) * S + i] = -INFINITY;
-        }
-        continue;
-      }
-      const RowSpan sp = row_span(a.mask, min(i, S - 1));
-      MapCursor mcur;
-      float m_run = -INFINITY;
-      float l_run = 0.f;
-      auto tile_step = [&](int n, auto idle_c) {
-        constexpr bool IDLE = decltype(idle_c)::value;
-        const int gn = g + n;
-        const int st = gn % NSB;             // S buffer
-        const uint32_t ph = (gn / NSB) & 1;
-        const int rp = (x + n) & 1;          // exchange parity
-        float s[64];
-        float mx = -INFINITY;
-        if constexpr (!IDLE) {
-          const int kt = __ldg(pl.kt_idx + w.beg + n);
-          const int e = __ldg(pl.kt_cls + w.beg + n);
-          const int c0 = kt * BN + half * 64;
-          const bool masked = entry_class(e) != LCA_TILE_FULL || kt * BN + BN > S;
-          uint32_t bits[2] = {0u, 0u};
-          if (masked && i < S) row_tile_bits<2>(a.mask, w.hm, i, c0, sp, bits, &mcur);
-          mbar_wait(&bar.s_full[st], ph, wc);
-          __syncwarp();
-          tc_fence_after();
-          uint32_t r[64];
-          tmem_ld64(lane_addr + TM_S0 + st * BN, r);
-#pragma unroll
-          for (int xx = 0; xx < 64; ++xx) s[xx] = __uint_as_float(r[xx]);
-          if (masked) {
-#pragma unroll
-            for (int xx = 0; xx < 64; ++xx)
-              if (!((bits[xx >> 5] >> (xx & 31)) & 1u)) s[xx] = -INFINITY;
-          }
-          float mq[8];
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) mq[kk] = s[kk];
-#pragma unroll
-          for (int xx = 8; xx < 64; xx += 8)
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) mq[kk] = fmaxf(mq[kk], s[xx + kk]);
-          mx = fmaxf(fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])),
-                     fmaxf(fmaxf(mq[4], mq[5]), fmaxf(mq[6], mq[7])));
-        } else {
-          mbar_wait(&bar.s_full[st], ph, wc);
-        }
-        red[(rp * 2 + half) * BM + t] = mx;
-        named_bar_sync(BAR_SOFTMAX, SOFTMAX_THREADS);
-        mx = fmaxf(mx, red[(rp * 2 + (half ^ 1)) * BM + t]);
-        const float mt = mx * sl2;
-        float alpha = 1.f;
-        bool rescale = false;
-        if (mt > m_run + RESCALE_THRESHOLD) {
-          rescale = (m_run != -INFINITY);
-          alpha = ex2_approx(m_run - mt);
-          l_run *= alpha;
-          m_run = mt;
-        }
-        if (__any_sync(0xFFFFFFFFu, rescale)) {
-          // O holds this unit's P V so far: wait for its last PV, scale, store back
-          const int pj = gn - 1;
-          mbar_wait(&bar.pv_done[pj % NSB], (pj / NSB) & 1, wc);
-          __syncwarp();
-          tc_fence_after();
-          const float f = rescale ? alpha : 1.f;
-          uint32_t o[OCOLS];
-          tmem_ldn<OCOLS>(quarter_addr + TM_O + half * OCOLS, o);
-#pragma unroll
-          for (int xx = 0; xx < OCOLS; ++xx) o[xx] = __float_as_uint(__uint_as_float(o[xx]) * f);
-          tmem_stn<OCOLS>(quarter_addr + TM_O + half * OCOLS, o);
-        }
-        if constexpr (!IDLE) {
-          const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-          float ls[8];
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) ls[kk] = 0.f;
-#pragma unroll
-          for (int xx = 0; xx < 64; ++xx) {
-            s[xx] = ex2_approx(fmaf(s[xx], sl2, -m_use));
-            ls[xx & 7] += s[xx];
-          }
-          l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
-          uint32_t pk[32];
-#pragma unroll
-          for (int xx = 0; xx < 32; ++xx) pk[xx] = pack_bf16x2(s[2 * xx], s[2 * xx + 1]);
-          tmem_st32(quarter_addr + TM_S0 + st * BN + half * 32, pk);
-        }
-        tc_fence_before();
-        mbar_arrive(&bar.p_ready[st]);
-      };
-      if (!use_half_path(pl.kt_cls + w.beg, w.n, HALF_SHARE, lane)) {
-        for (int n = 0; n < w.n; ++n) tile_step(n, std::false_type{});
-      } else {
-        for (int n = 0; n < w.n; ++n) {
-          if ((entry_empty_halves(__ldg(pl.kt_cls + w.beg + n)) >> half) & 1)
-            tile_step(n, std::true_type{});
-          else
-            tile_step(n, std::false_type{});
-        }
-      }
+    int xc = 0;   // row-max / row-sum exchanges so far; its parity picks the red half
 
-      // ---- epilogue: O = acc / l (bf16), LSE = (m + log2 l) * ln 2; then O is free
-      {
-        const int pj = g + w.n - 1;
+    // This thread's row of one unit: running max (log2 units) and sum, allowed key span,
+    // block-map search hints.
+    struct RowState {
+      float m_run, l_run;
+      RowSpan sp;
+      MapCursor mcur;
+    };
+    auto start_row = [&](const Unit& w, RowState& rs) {
+      rs.m_run = -INFINITY;
+      rs.l_run = 0.f;
+      rs.sp = row_span(a.mask, min(w.qt * BM + t, S - 1));
+      rs.mcur = MapCursor{};
+    };
+    // Key tile n of unit w, whose tiles start at tile counter g0; IDLE: this warp's key
+    // half holds no pair of the tile (only the barrier protocol).
+    auto tile_step = [&](const Unit& w, int g0, int n, RowState& rs, auto idle_c) {
+      constexpr bool IDLE = decltype(idle_c)::value;
+      const int i = w.qt * BM + t;
+      const int gn = g0 + n;
+      const int st = gn % NSB;             // S buffer
+      const uint32_t ph = (gn / NSB) & 1;
+      const int rp = xc & 1;
+      ++xc;
+      float s[64];
+      float mx = -INFINITY;
+      if constexpr (!IDLE) {
+        const int kt = __ldg(pl.kt_idx + w.beg + n);
+        const int e = __ldg(pl.kt_cls + w.beg + n);
+        const int c0 = kt * BN + half * 64;
+        const bool masked = entry_class(e) != LCA_TILE_FULL || kt * BN + BN > S;
+        uint32_t bits[2] = {0u, 0u};
+        if (masked && i < S) row_tile_bits<2>(a.mask, w.hm, i, c0, rs.sp, bits, &rs.mcur);
+        mbar_wait(&bar.s_full[st], ph, wc);
+        __syncwarp();
+        tc_fence_after();
+        uint32_t r[64];
+        tmem_ld64(lane_addr + TM_S0 + st * BN, r);
+#pragma unroll
+        for (int xx = 0; xx < 64; ++xx) s[xx] = __uint_as_float(r[xx]);
+        if (masked) {
+#pragma unroll
+          for (int xx = 0; xx < 64; ++xx)
+            if (!((bits[xx >> 5] >> (xx & 31)) & 1u)) s[xx] = -INFINITY;
+        }
+        float mq[8];
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) mq[kk] = s[kk];
+#pragma unroll
+        for (int xx = 8; xx < 64; xx += 8)
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) mq[kk] = fmaxf(mq[kk], s[xx + kk]);
+        mx = fmaxf(fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])),
+                   fmaxf(fmaxf(mq[4], mq[5]), fmaxf(mq[6], mq[7])));
+      } else {
+        mbar_wait(&bar.s_full[st], ph, wc);
+      }
+      red[(rp * 2 + half) * BM + t] = mx;
+      named_bar_sync(BAR_SOFTMAX, SOFTMAX_THREADS);
+      mx = fmaxf(mx, red[(rp * 2 + (half ^ 1)) * BM + t]);
+      const float mt = mx * sl2;
+      float alpha = 1.f;
+      bool rescale = false;
+      if (mt > rs.m_run + RESCALE_THRESHOLD) {
+        rescale = (rs.m_run != -INFINITY);
+        alpha = ex2_approx(rs.m_run - mt);
+        rs.l_run *= alpha;
+        rs.m_run = mt;
+      }
+      // never on a unit's first tile (m_run starts at -inf), so never while O still holds
+      // the previous unit's result
+      if (__any_sync(0xFFFFFFFFu, rescale)) {
+        // O holds this unit's P V so far: wait for its last PV, scale, store back
+        const int pj = gn - 1;
         mbar_wait(&bar.pv_done[pj % NSB], (pj / NSB) & 1, wc);
         __syncwarp();
         tc_fence_after();
+        const float f = rescale ? alpha : 1.f;
+        uint32_t o[OCOLS];
+        tmem_ldn<OCOLS>(quarter_addr + TM_O + half * OCOLS, o);
+#pragma unroll
+        for (int xx = 0; xx < OCOLS; ++xx) o[xx] = __float_as_uint(__uint_as_float(o[xx]) * f);
+        tmem_stn<OCOLS>(quarter_addr + TM_O + half * OCOLS, o);
       }
-      const int pe = (x + w.n) & 1;
-      red[(pe * 2 + half) * BM + t] = l_run;
+      if constexpr (!IDLE) {
+        const float m_use = (rs.m_run == -INFINITY) ? 0.f : rs.m_run;
+        float ls[8];
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) ls[kk] = 0.f;
+#pragma unroll
+        for (int xx = 0; xx < 64; ++xx) {
+          s[xx] = ex2_approx(fmaf(s[xx], sl2, -m_use));
+          ls[xx & 7] += s[xx];
+        }
+        rs.l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+        uint32_t pk[32];
+#pragma unroll
+        for (int xx = 0; xx < 32; ++xx) pk[xx] = pack_bf16x2(s[2 * xx], s[2 * xx + 1]);
+        tmem_st32(quarter_addr + TM_S0 + st * BN + half * 32, pk);
+      }
+      tc_fence_before();
+      mbar_arrive(&bar.p_ready[st]);
+    };
+    // tiles [n0, w.n) of unit w; rows whose list runs the half-width path check each
+    // tile's flags, the others run the loop without any flag handling
+    auto run_tiles = [&](const Unit& w, int g0, int n0, RowState& rs) {
+      if (!w.halves) {
+        for (int n = n0; n < w.n; ++n) tile_step(w, g0, n, rs, std::false_type{});
+      } else {
+        for (int n = n0; n < w.n; ++n) {
+          if ((entry_empty_halves(__ldg(pl.kt_cls + w.beg + n)) >> half) & 1)
+            tile_step(w, g0, n, rs, std::true_type{});
+          else
+            tile_step(w, g0, n, rs, std::false_type{});
+        }
+      }
+    };
+    // Epilogue, first part (no wait on the MMAs): l over the whole row, LSE =
+    // (m + log2 l) * ln 2 stored; returns 1 / l (0 for a row without allowed keys).
+    auto epilogue_sum = [&](const Unit& w, const RowState& rs) {
+      const int i = w.qt * BM + t;
+      const int pe = xc & 1;
+      ++xc;
+      red[(pe * 2 + half) * BM + t] = rs.l_run;
       named_bar_sync(BAR_SOFTMAX, SOFTMAX_THREADS);
-      const float l_tot = l_run + red[(pe * 2 + (half ^ 1)) * BM + t];
-      const float inv = (l_tot > 0.f) ? 1.f / l_tot : 0.f;
+      const float l_tot = rs.l_run + red[(pe * 2 + (half ^ 1)) * BM + t];
+      if (i < S && half == 0) {
+        const float lse = (l_tot > 0.f) ? (rs.m_run + __log2f(l_tot)) * 0.69314718055994531f
+                                        : -INFINITY;
+        a.lse[(static_cast<int64_t>(w.b) * dm.h_q + w.h) * S + i] = lse;
+      }
+      return (l_tot > 0.f) ? 1.f / l_tot : 0.f;
+    };
+    // Epilogue, second part: after the unit's last PV, O = acc / l (bf16) to orow (null
+    // past S); then O is free for the next unit.
+    auto epilogue_out = [&](int last_tile, float inv, __nv_bfloat16* orow) {
+      mbar_wait(&bar.pv_done[last_tile % NSB], (last_tile / NSB) & 1, wc);
+      __syncwarp();
+      tc_fence_after();
       uint32_t o[OCOLS];
       tmem_ldn<OCOLS>(quarter_addr + TM_O + half * OCOLS, o);
       tc_fence_before();
       mbar_arrive(&bar.o_free);
-      if (i < S) {
-        __nv_bfloat16* orow = a.o + (static_cast<int64_t>(w.b) * S + i) * a.o_row_stride +
-                              static_cast<int64_t>(w.h) * HD + half * OCOLS;
+      if (orow != nullptr) {
         uint4* dst = reinterpret_cast<uint4*>(orow);
 #pragma unroll
         for (int v = 0; v < OCOLS / 8; ++v) {
@@ -556,17 +606,58 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           ww.w = pack_bf16x2(__uint_as_float(o[xx + 6]) * inv, __uint_as_float(o[xx + 7]) * inv);
           dst[v] = ww;
         }
-        if (half == 0) {
-          const float lse = (l_tot > 0.f) ? (m_run + __log2f(l_tot)) * 0.69314718055994531f
-                                          : -INFINITY;
-          a.lse[(static_cast<int64_t>(w.b) * dm.h_q + w.h) * S + i] = lse;
-        }
       }
+    };
+
+    // Unit transitions: the next unit's row set-up and first tile run between the two
+    // parts of the current unit's epilogue.  Its S is computed by then (the MMA warp
+    // issues a unit's first S MMAs as soon as its Q has landed), and the first tile never
+    // touches O, so the wait for the last PV and the set-up's global loads overlap work
+    // the tensor pipe can use.
+    int g = 0;    // tile counter (S buffers, barrier phases)
+    int k = 0;
+    Unit w = take_unit(0, true);
+    RowState rs{};
+    bool started = false;   // rs holds w's row and w's first tile has run
+    while (w.n >= 0) {
+      if (w.n == 0) {   // no allowed key anywhere in the tile: O = 0, LSE = -inf
+        const int i = w.qt * BM + t;
+        if (i < S) {
+          uint4* dst = reinterpret_cast<uint4*>(a.o + (static_cast<int64_t>(w.b) * S + i) *
+                                                          a.o_row_stride +
+                                                static_cast<int64_t>(w.h) * HD + half * OCOLS);
+#pragma unroll
+          for (int v = 0; v < OCOLS / 8; ++v) dst[v] = make_uint4(0u, 0u, 0u, 0u);
+          if (half == 0) a.lse[(static_cast<int64_t>(w.b) * dm.h_q + w.h) * S + i] = -INFINITY;
+        }
+        w = take_unit(++k, true);
+        started = false;
+        continue;
+      }
+      if (!started) start_row(w, rs);
+      run_tiles(w, g, started ? 1 : 0, rs);   // one call site: one copy of the loops
+      const float inv = epilogue_sum(w, rs);
+      const int iw = w.qt * BM + t;
+      __nv_bfloat16* orow = iw < S ? a.o + (static_cast<int64_t>(w.b) * S + iw) * a.o_row_stride +
+                                         static_cast<int64_t>(w.h) * HD + half * OCOLS
+                                   : nullptr;
+      const int last_tile = g + w.n - 1;
+      const Unit wn = take_unit(++k, true);
+      RowState rn{};
+      started = false;
+      if (wn.n > 0) {
+        // a tile with an empty key half is partial, so this warp's half is masked out
+        // in full there: the full-width step is correct for it too
+        start_row(wn, rn);
+        tile_step(wn, g + w.n, 0, rn, std::false_type{});
+        started = true;
+      }
+      epilogue_out(last_tile, inv, orow);
       g += w.n;
-      x += w.n + 1;
+      w = wn;
+      rs = rn;
     }
   }
-
   tc_fence_before();
   __syncthreads();
   if (warp == WARP_MMA) {
