@@ -93,6 +93,10 @@ def heterogeneous_cases(s):
             Case("BLOCK_CAUSAL_DOCUMENT",
                  lambda st: I.make_desc(I.BLOCK_CAUSAL_DOCUMENT, s, block=2048, doc_seed=st),
                  True),
+            # the block size the pages' own measurement section gives for this mask
+            Case("BLOCK_CAUSAL_DOCUMENT_Bk1024",
+                 lambda st: I.make_desc(I.BLOCK_CAUSAL_DOCUMENT, s, block=1024, doc_seed=st),
+                 True),
             Case("SLIDING_WINDOW_DOCUMENT",
                  lambda st: I.make_desc(I.SLIDING_WINDOW_DOCUMENT, s, window=1024, doc_seed=st),
                  True)]
@@ -145,9 +149,9 @@ def _workload(suite, case=None):
         return ([(32768, 64, 64, heterogeneous_cases(32768))],
                 "heterogeneous static masks, S=32K, MHA 64:64, d=128: PREFIX_LM (prefix 8K), "
                 "SHARED_QUESTION (2K question + 4 x 7.5K answers), GLOBAL_SLIDING (256 global, "
-                "w=4096), CAUSAL_BLOCKWISE (2K blocks), BLOCK_CAUSAL_DOCUMENT (2K blocks in "
-                "lognormal documents); plus the sliding window (w=1024) inside lognormal "
-                "documents")
+                "w=4096), CAUSAL_BLOCKWISE (2K blocks), BLOCK_CAUSAL_DOCUMENT (2K and 1K "
+                "blocks in lognormal documents); plus the sliding window (w=1024) inside "
+                "lognormal documents")
     if suite == "sparse":
         groups = []
         for s in (32768, 65536, 131072):
